@@ -1,0 +1,339 @@
+"""Block-scaled weight conversion on GB300: Python binding of libmxq.
+
+Argument marshalling only.  Every conversion runs in the CUDA kernels of
+``libmxq.so`` (built from ``csrc/`` by ``build.py``) through its C ABI
+(``include/mxq.h``); PyTorch supplies device memory and the current stream.
+There is no CPU path: if the library is missing the call raises.
+
+Functions carry the C names:
+
+* ``mxq_fake_quant_mxfp4``     MXFP4 projection (TE PR #3264, mode 1)
+* ``mxq_mxfp8_row_direct``     direct MXFP8 rowwise (TE PR #3264, mode 2)
+* ``mxq_fp8_block128_direct``  direct FP8 128x128 blockwise (TE PR #3264, mode 2)
+* ``mxq_dequantize``           MXFP8 rowwise / 128x128 blockwise -> bf16 / fp32
+* ``mxq_export_mxfp8``         export_components (TE PR #3790)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import NamedTuple, Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "MXQError", "MXFP8Components", "Library", "library",
+    "mxq_fake_quant_mxfp4", "mxq_mxfp8_row_direct", "mxq_fp8_block128_direct",
+    "mxq_dequantize", "mxq_export_mxfp8", "mxq_scale_bytes", "mxq_tile_scale_count",
+    "COMPACT", "PADDED", "SWIZZLED", "scale_cols",
+]
+
+COMPACT, PADDED, SWIZZLED = 0, 1, 2
+_LAYOUTS = {"compact": COMPACT, "padded": PADDED, "swizzled": SWIZZLED, COMPACT: COMPACT, PADDED: PADDED,
+            SWIZZLED: SWIZZLED}
+_BF16, _FP32, _FP16 = 0, 1, 2
+_E4M3, _E5M2 = 0, 1
+_MXFP8_ROW, _BLOCK128 = 0, 1
+
+
+class MXQError(RuntimeError):
+    def __init__(self, status: int, msg: str, where: str):
+        super().__init__(f"{where}: {msg} (mxq status {status})")
+        self.status = status
+
+
+class MXFP8Components(NamedTuple):
+    """Exported MXFP8 values and compact E8M0 scales (TE PR #3790)."""
+    data: torch.Tensor       # float8_e4m3fn / float8_e5m2 view of the payload
+    scale_inv: torch.Tensor  # uint8 (*shape[:-1], ceil(K/32))
+    is_view: bool            # True if scale_inv aliases the storage's scales
+
+
+class _Quantized(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("data", ctypes.c_void_p), ("rows", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("fp8", ctypes.c_int), ("scales", ctypes.c_void_p), ("lay", ctypes.c_int),
+                ("tile_scale_inv", ctypes.c_void_p)]
+
+
+class _Storage(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("fp8", ctypes.c_int), ("lay", ctypes.c_int),
+                ("rows", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class _Components(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("fp8", ctypes.c_int), ("scales", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("K", ctypes.c_int64), ("scale_cols", ctypes.c_int64),
+                ("is_view", ctypes.c_int)]
+
+
+def scale_cols(K: int) -> int:
+    return (K + 31) // 32
+
+
+def _dt_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _BF16
+    if t.dtype == torch.float32:
+        return _FP32
+    if t.dtype == torch.float16:
+        return _FP16
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32 expected")
+
+
+def _fp8_code(fp8) -> int:
+    if fp8 in ("e4m3", torch.float8_e4m3fn, _E4M3):
+        return _E4M3
+    if fp8 in ("e5m2", torch.float8_e5m2, _E5M2):
+        return _E5M2
+    raise ValueError(f"unknown fp8 kind {fp8!r}")
+
+
+def _rows_view(x: torch.Tensor):
+    """(rows, K, ld) of x seen as rows of its last dimension, without a copy."""
+    if x.dim() == 0:
+        raise ValueError("need at least one dimension")
+    K = x.shape[-1]
+    if x.dim() == 1:
+        if K > 1 and x.stride(0) != 1:
+            raise ValueError("last dimension must be contiguous")
+        return 1, K, K
+    if x.numel() == 0:
+        rows = 1
+        for d in x.shape[:-1]:
+            rows *= d
+        return rows, K, K
+    if K > 1 and x.stride(-1) != 1:
+        raise ValueError("last dimension must be contiguous")
+    try:
+        v = x.view(-1, K)
+    except RuntimeError as exc:
+        raise ValueError("leading dimensions must flatten to one row stride (no copy is made)") from exc
+    ld = v.stride(0) if v.shape[0] > 1 else K
+    return v.shape[0], K, max(ld, K)
+
+
+def _stream(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libmxq works on CUDA tensors only")
+
+
+class Library:
+    """One loaded libmxq variant (``fastmath=True`` loads the --use_fast_math build)."""
+
+    def __init__(self, fastmath: bool = False, build: bool = True):
+        name = "libmxq_fastmath.so" if fastmath else "libmxq.so"
+        path = _build.lib_path(name)
+        if build:
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with python -m block_scaled_precision_x32_gb300.build")
+        self.path = path
+        L = ctypes.CDLL(path)
+        i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        L.mxq_fake_quant_mxfp4.argtypes = [vp, vp, ci, i64, i64, i64, i64, vp]
+        L.mxq_mxfp8_row_direct.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp]
+        L.mxq_fp8_block128_direct.argtypes = [vp, ci, i64, i64, i64, vp, vp, vp]
+        L.mxq_dequantize.argtypes = [ctypes.POINTER(_Quantized), vp, ci, vp]
+        L.mxq_export_mxfp8.argtypes = [ctypes.POINTER(_Storage), vp, ctypes.c_size_t, ctypes.POINTER(_Components), vp]
+        L.mxq_scale_bytes.argtypes = [i64, i64, ci]
+        L.mxq_scale_bytes.restype = ctypes.c_size_t
+        L.mxq_tile_scale_count.argtypes = [i64, i64]
+        L.mxq_tile_scale_count.restype = ctypes.c_size_t
+        L.mxq_status_string.argtypes = [ci]
+        L.mxq_status_string.restype = ctypes.c_char_p
+        for fn in ("mxq_fake_quant_mxfp4", "mxq_mxfp8_row_direct", "mxq_fp8_block128_direct", "mxq_dequantize",
+                   "mxq_export_mxfp8"):
+            getattr(L, fn).restype = ci
+        self.L = L
+
+    def _check(self, status: int, where: str):
+        if status != 0:
+            raise MXQError(status, self.L.mxq_status_string(status).decode(), where)
+
+    # -- sizes ----------------------------------------------------------
+    def scale_bytes(self, rows: int, K: int, layout="compact") -> int:
+        return int(self.L.mxq_scale_bytes(rows, K, _LAYOUTS[layout]))
+
+    def tile_scale_count(self, rows: int, K: int) -> int:
+        return int(self.L.mxq_tile_scale_count(rows, K))
+
+    # -- conversions ----------------------------------------------------
+    def fake_quant_mxfp4(self, x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        _need_cuda(x, out)
+        dt = _dt_code(x)
+        rows, K, ldx = _rows_view(x)
+        if out is None:
+            out = torch.empty_like(x, memory_format=torch.contiguous_format)
+        if out.shape != x.shape or out.dtype != x.dtype:
+            raise ValueError("out must match x in shape and dtype")
+        _, _, ldy = _rows_view(out)
+        with torch.cuda.device(x.device):
+            self._check(self.L.mxq_fake_quant_mxfp4(x.data_ptr(), out.data_ptr(), dt, rows, K, ldx, ldy,
+                                                    _stream(x)), "mxq_fake_quant_mxfp4")
+        return out
+
+    def mxfp8_row_direct(self, x: torch.Tensor, layout="compact", data: Optional[torch.Tensor] = None,
+                         scales: Optional[torch.Tensor] = None):
+        """Returns (payload uint8 of x's shape, scales).  Compact scales are
+        shaped (*shape[:-1], nb); padded and swizzled ones (Rp, Cp)."""
+        _need_cuda(x, data, scales)
+        dt = _dt_code(x)
+        lay = _LAYOUTS[layout]
+        rows, K, ldx = _rows_view(x)
+        nb = scale_cols(K)
+        if data is None:
+            data = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        if scales is None:
+            if lay == COMPACT:
+                scales = torch.empty(tuple(x.shape[:-1]) + (nb,), dtype=torch.uint8, device=x.device)
+            else:
+                scales = torch.empty(((rows + 127) // 128 * 128, (nb + 3) // 4 * 4), dtype=torch.uint8,
+                                     device=x.device)
+        if not data.is_contiguous() or data.numel() != rows * K or data.dtype != torch.uint8:
+            raise ValueError("data must be a contiguous uint8 tensor of rows*K bytes")
+        if not scales.is_contiguous() or scales.numel() < self.scale_bytes(rows, K, lay):
+            raise ValueError("scales buffer too small or not contiguous")
+        with torch.cuda.device(x.device):
+            self._check(self.L.mxq_mxfp8_row_direct(x.data_ptr(), dt, rows, K, ldx, data.data_ptr(),
+                                                    scales.data_ptr(), lay, _stream(x)), "mxq_mxfp8_row_direct")
+        return data, scales
+
+    def fp8_block128_direct(self, x: torch.Tensor, data: Optional[torch.Tensor] = None,
+                            tile_scale_inv: Optional[torch.Tensor] = None):
+        """Returns (E4M3 payload uint8 of x's shape, fp32 2^T per 128x128 tile)."""
+        _need_cuda(x, data, tile_scale_inv)
+        dt = _dt_code(x)
+        rows, K, ldx = _rows_view(x)
+        if data is None:
+            data = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        if tile_scale_inv is None:
+            tile_scale_inv = torch.empty(((rows + 127) // 128, (K + 127) // 128), dtype=torch.float32,
+                                         device=x.device)
+        if not data.is_contiguous() or data.numel() != rows * K:
+            raise ValueError("data must be a contiguous uint8 tensor of rows*K bytes")
+        if tile_scale_inv.dtype != torch.float32 or tile_scale_inv.numel() < self.tile_scale_count(rows, K):
+            raise ValueError("tile_scale_inv must be fp32 with ceil(rows/128)*ceil(K/128) entries")
+        with torch.cuda.device(x.device):
+            self._check(self.L.mxq_fp8_block128_direct(x.data_ptr(), dt, rows, K, ldx, data.data_ptr(),
+                                                       tile_scale_inv.data_ptr(), _stream(x)),
+                        "mxq_fp8_block128_direct")
+        return data, tile_scale_inv
+
+    def dequantize(self, data: torch.Tensor, *, scales: Optional[torch.Tensor] = None, layout="compact",
+                   fp8="e4m3", tile_scale_inv: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """MXFP8 rowwise (pass ``scales``) or 128x128 blockwise (pass
+        ``tile_scale_inv``) payload -> bf16 / fp32 of data's shape."""
+        _need_cuda(data, scales, tile_scale_inv, out)
+        if (scales is None) == (tile_scale_inv is None):
+            raise ValueError("pass exactly one of scales (MXFP8 rowwise) or tile_scale_inv (128x128)")
+        if not data.is_contiguous():
+            raise ValueError("data must be contiguous")
+        K = data.shape[-1] if data.dim() else 1
+        rows = data.numel() // K if K else 0
+        q = _Quantized()
+        q.kind = _MXFP8_ROW if scales is not None else _BLOCK128
+        q.data = data.data_ptr()
+        q.rows, q.K = rows, K
+        q.fp8 = _fp8_code(fp8)
+        q.lay = _LAYOUTS[layout]
+        q.scales = scales.data_ptr() if scales is not None else None
+        q.tile_scale_inv = tile_scale_inv.data_ptr() if tile_scale_inv is not None else None
+        if out is None:
+            out = torch.empty(data.shape, dtype=out_dtype, device=data.device)
+        if not out.is_contiguous() or out.shape != data.shape:
+            raise ValueError("out must be contiguous with data's shape")
+        if out.dtype == torch.float16:
+            odt = _FP16
+        else:
+            odt = _dt_code(out)
+        with torch.cuda.device(data.device):
+            self._check(self.L.mxq_dequantize(ctypes.byref(q), out.data_ptr(), odt, _stream(data)),
+                        "mxq_dequantize")
+        return out
+
+    def export_mxfp8(self, data: Optional[torch.Tensor], scales: torch.Tensor, *, shape, layout="compact",
+                     fp8="e4m3", scale_out: Optional[torch.Tensor] = None) -> MXFP8Components:
+        """export_components of an MXFP8 storage whose rowwise payload is
+        ``data`` (None = no row-scaled data) and whose scales are held in
+        ``layout``."""
+        shape = tuple(shape)
+        K = shape[-1] if shape else 0
+        rows = 1
+        for d in shape[:-1]:
+            rows *= d
+        nb = scale_cols(K)
+        dev = scales.device
+        _need_cuda(scales, data, scale_out)
+        st = _Storage()
+        st.data = data.data_ptr() if data is not None else None
+        st.scales = scales.data_ptr()
+        st.fp8 = _fp8_code(fp8)
+        st.lay = _LAYOUTS[layout]
+        st.rows, st.K = rows, K
+        if scale_out is None:
+            view = st.lay == COMPACT or (st.lay == PADDED and nb % 4 == 0) or rows * K == 0
+            if not view:
+                scale_out = torch.empty(rows * nb, dtype=torch.uint8, device=dev)
+        comp = _Components()
+        with torch.cuda.device(dev):
+            self._check(self.L.mxq_export_mxfp8(ctypes.byref(st), scale_out.data_ptr() if scale_out is not None else None,
+                                                scale_out.numel() if scale_out is not None else 0, ctypes.byref(comp),
+                                                _stream(scales)), "mxq_export_mxfp8")
+        fp8_dtype = torch.float8_e4m3fn if st.fp8 == _E4M3 else torch.float8_e5m2
+        values = data.view(fp8_dtype).view(shape) if data is not None else None
+        if comp.is_view:
+            s = scales.reshape(-1)[: rows * nb].view(shape[:-1] + (nb,))
+        else:
+            s = scale_out.reshape(-1)[: rows * nb].view(shape[:-1] + (nb,))
+        return MXFP8Components(values, s, bool(comp.is_view))
+
+
+_default: Optional[Library] = None
+_lock = threading.Lock()
+
+
+def library() -> Library:
+    """The default libmxq, built in-tree on first use."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Library()
+    return _default
+
+
+def mxq_fake_quant_mxfp4(x, out=None):
+    return library().fake_quant_mxfp4(x, out)
+
+
+def mxq_mxfp8_row_direct(x, layout="compact", data=None, scales=None):
+    return library().mxfp8_row_direct(x, layout, data, scales)
+
+
+def mxq_fp8_block128_direct(x, data=None, tile_scale_inv=None):
+    return library().fp8_block128_direct(x, data, tile_scale_inv)
+
+
+def mxq_dequantize(data, **kw):
+    return library().dequantize(data, **kw)
+
+
+def mxq_export_mxfp8(data, scales, **kw):
+    return library().export_mxfp8(data, scales, **kw)
+
+
+def mxq_scale_bytes(rows, K, layout="compact"):
+    return library().scale_bytes(rows, K, layout)
+
+
+def mxq_tile_scale_count(rows, K):
+    return library().tile_scale_count(rows, K)

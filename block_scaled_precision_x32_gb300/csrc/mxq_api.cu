@@ -1,0 +1,206 @@
+// mxq_api.cu -- the C entry points of libmxq: host-side argument checks,
+// then one kernel launch on the caller's stream.  Declared and documented
+// in include/mxq.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/mxq.h"
+#include "mxq_internal.h"
+
+namespace mxq {
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+    const int slot = dev < 64 ? dev : 63;
+    if (cached[slot] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+        cached[slot] = n;
+    }
+    return cached[slot];
+}
+
+}  // namespace mxq
+
+namespace {
+
+bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+mxq_status check_dtype(mxq_dtype dt) {
+    if (dt == MXQ_BF16 || dt == MXQ_FP32) return MXQ_OK;
+    if (dt == MXQ_FP16) return MXQ_ERR_UNSUPPORTED_DTYPE;
+    return MXQ_ERR_INVALID_ARG;
+}
+
+size_t elt_size(mxq_dtype dt) { return dt == MXQ_BF16 ? 2 : 4; }
+
+bool valid_layout(mxq_scale_layout lay) {
+    return lay == MXQ_SCALES_COMPACT || lay == MXQ_SCALES_PADDED || lay == MXQ_SCALES_SWIZZLED;
+}
+
+// rows, K >= 0; ld >= K; the byte span of the view fits in int64.
+bool valid_shape(int64_t rows, int64_t K, int64_t ld) {
+    if (rows < 0 || K < 0 || ld < K) return false;
+    if (rows > 0 && ld > (INT64_C(1) << 40)) return false;
+    if (rows > (INT64_C(1) << 40) || K > (INT64_C(1) << 40)) return false;
+    return true;
+}
+
+mxq_status launch_status(cudaError_t e) { return e == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA; }
+
+mxq::Elt elt_of(mxq_dtype dt) { return dt == MXQ_BF16 ? mxq::Elt::BF16 : mxq::Elt::FP32; }
+
+}  // namespace
+
+extern "C" {
+
+size_t mxq_scale_bytes(int64_t rows, int64_t K, mxq_scale_layout lay) {
+    if (rows <= 0 || K <= 0) return 0;
+    const int64_t nb = (K + 31) / 32;
+    if (lay == MXQ_SCALES_COMPACT) return (size_t)(rows * nb);
+    return (size_t)(((rows + 127) / 128 * 128) * ((nb + 3) / 4 * 4));
+}
+
+size_t mxq_tile_scale_count(int64_t rows, int64_t K) {
+    if (rows <= 0 || K <= 0) return 0;
+    return (size_t)(((rows + 127) / 128) * ((K + 127) / 128));
+}
+
+mxq_status mxq_fake_quant_mxfp4(const void* x, void* y, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                int64_t ldy, cudaStream_t stream) {
+    mxq_status st = check_dtype(dt);
+    if (st != MXQ_OK) return st;
+    if (!valid_shape(rows, K, ldx) || !valid_shape(rows, K, ldy)) return MXQ_ERR_INVALID_ARG;
+    if (rows == 0 || K == 0) return MXQ_OK;
+    if (!x || !y || !aligned(x, elt_size(dt)) || !aligned(y, elt_size(dt))) return MXQ_ERR_INVALID_ARG;
+    if (x == y && ldx != ldy) return MXQ_ERR_INVALID_ARG;
+    mxq::RowwiseArgs a{};
+    a.x = x;
+    a.y = y;
+    a.rows = rows;
+    a.K = K;
+    a.ldx = ldx;
+    a.ldy = ldy;
+    return launch_status(mxq::launch_rowwise(mxq::RowMode::PROJECT, elt_of(dt), a, stream));
+}
+
+mxq_status mxq_mxfp8_row_direct(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* data,
+                                uint8_t* scales, mxq_scale_layout lay, cudaStream_t stream) {
+    mxq_status st = check_dtype(dt);
+    if (st != MXQ_OK) return st;
+    if (!valid_shape(rows, K, ldx) || !valid_layout(lay)) return MXQ_ERR_INVALID_ARG;
+    if (rows == 0 || K == 0) return MXQ_OK;
+    if (!x || !data || !scales || !aligned(x, elt_size(dt))) return MXQ_ERR_INVALID_ARG;
+    mxq::RowwiseArgs a{};
+    a.x = x;
+    a.data = data;
+    a.scales = scales;
+    a.rows = rows;
+    a.K = K;
+    a.ldx = ldx;
+    a.ldy = K;
+    a.lay = (int)lay;
+    return launch_status(mxq::launch_rowwise(mxq::RowMode::MXFP8, elt_of(dt), a, stream));
+}
+
+mxq_status mxq_fp8_block128_direct(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* data,
+                                   float* tile_scale_inv, cudaStream_t stream) {
+    mxq_status st = check_dtype(dt);
+    if (st != MXQ_OK) return st;
+    if (!valid_shape(rows, K, ldx)) return MXQ_ERR_INVALID_ARG;
+    if (rows == 0 || K == 0) return MXQ_OK;
+    if (!x || !data || !tile_scale_inv || !aligned(x, elt_size(dt)) || !aligned(tile_scale_inv, 4))
+        return MXQ_ERR_INVALID_ARG;
+    mxq::Block128Args a{};
+    a.x = x;
+    a.data = data;
+    a.tile_scale_inv = tile_scale_inv;
+    a.rows = rows;
+    a.K = K;
+    a.ldx = ldx;
+    return launch_status(mxq::launch_block128(elt_of(dt), a, stream));
+}
+
+mxq_status mxq_dequantize(const mxq_quantized* q, void* out, mxq_dtype out_dt, cudaStream_t stream) {
+    if (!q) return MXQ_ERR_INVALID_ARG;
+    mxq_status st = check_dtype(out_dt);
+    if (st != MXQ_OK) return st;
+    if (!valid_shape(q->rows, q->K, q->K)) return MXQ_ERR_INVALID_ARG;
+    if (q->kind != MXQ_QUANT_MXFP8_ROW && q->kind != MXQ_QUANT_FP8_BLOCK128) return MXQ_ERR_INVALID_ARG;
+    if (q->fp8 != MXQ_E4M3 && q->fp8 != MXQ_E5M2) return MXQ_ERR_INVALID_ARG;
+    if (q->kind == MXQ_QUANT_FP8_BLOCK128 && q->fp8 != MXQ_E4M3) return MXQ_ERR_INVALID_ARG;
+    if (q->kind == MXQ_QUANT_MXFP8_ROW && !valid_layout(q->lay)) return MXQ_ERR_INVALID_ARG;
+    if (q->rows == 0 || q->K == 0) return MXQ_OK;
+    if (!q->data || !out || !aligned(out, elt_size(out_dt))) return MXQ_ERR_INVALID_ARG;
+    if (q->kind == MXQ_QUANT_MXFP8_ROW && !q->scales) return MXQ_ERR_INVALID_ARG;
+    if (q->kind == MXQ_QUANT_FP8_BLOCK128 && (!q->tile_scale_inv || !aligned(q->tile_scale_inv, 4)))
+        return MXQ_ERR_INVALID_ARG;
+    mxq::DequantArgs a{};
+    a.kind = (int)q->kind;
+    a.data = q->data;
+    a.rows = q->rows;
+    a.K = q->K;
+    a.fp8 = (int)q->fp8;
+    a.scales = q->scales;
+    a.lay = (int)q->lay;
+    a.tile_scale_inv = q->tile_scale_inv;
+    a.out = out;
+    a.out_bf16 = out_dt == MXQ_BF16;
+    return launch_status(mxq::launch_dequant(a, stream));
+}
+
+mxq_status mxq_export_mxfp8(const mxq_mxfp8_storage* st, uint8_t* scale_out, size_t scale_out_bytes,
+                            mxq_mxfp8_components* out, cudaStream_t stream) {
+    if (!st || !out) return MXQ_ERR_INVALID_ARG;
+    if (!valid_shape(st->rows, st->K, st->K) || !valid_layout(st->lay)) return MXQ_ERR_INVALID_ARG;
+    if (st->fp8 != MXQ_E4M3 && st->fp8 != MXQ_E5M2) return MXQ_ERR_INVALID_ARG;
+    const int64_t nb = (st->K + 31) / 32;
+    const bool empty = st->rows == 0 || st->K == 0;
+    if (!st->data && !empty) return MXQ_ERR_NO_ROWWISE_DATA;
+    if (!st->scales && !empty) return MXQ_ERR_INVALID_ARG;
+    mxq_mxfp8_components c{};
+    c.data = st->data;
+    c.fp8 = st->fp8;
+    c.rows = st->rows;
+    c.K = st->K;
+    c.scale_cols = nb;
+    const bool view = st->lay == MXQ_SCALES_COMPACT || (st->lay == MXQ_SCALES_PADDED && nb % 4 == 0);
+    if (empty || view) {
+        c.scales = st->scales;
+        c.is_view = 1;
+        *out = c;
+        return MXQ_OK;
+    }
+    if (!scale_out || scale_out_bytes < (size_t)(st->rows * nb)) return MXQ_ERR_BUFFER_TOO_SMALL;
+    mxq::ExportArgs a{};
+    a.scales = st->scales;
+    a.lay = (int)st->lay;
+    a.rows = st->rows;
+    a.K = st->K;
+    a.out = scale_out;
+    const mxq_status ls = launch_status(mxq::launch_export(a, stream));
+    if (ls != MXQ_OK) return ls;
+    c.scales = scale_out;
+    c.is_view = 0;
+    *out = c;
+    return MXQ_OK;
+}
+
+const char* mxq_status_string(mxq_status s) {
+    switch (s) {
+        case MXQ_OK: return "ok";
+        case MXQ_ERR_INVALID_ARG: return "invalid argument";
+        case MXQ_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype (fp16 is rejected)";
+        case MXQ_ERR_NO_ROWWISE_DATA: return "tensor has no row-scaled data";
+        case MXQ_ERR_BUFFER_TOO_SMALL: return "scale output buffer too small";
+        case MXQ_ERR_CUDA: return "CUDA launch failed";
+    }
+    return "unknown status";
+}
+
+int mxq_version(void) { return MXQ_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// mxq_internal.h -- host-side launchers shared between the C entry points
+// (mxq_api.cu) and the kernel translation units.  Not part of the ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime_api.h>
+
+namespace mxq {
+
+enum class Elt { BF16, FP32 };
+enum class RowMode { PROJECT, MXFP8 };
+
+struct RowwiseArgs {
+    const void* x;
+    void* y;          // PROJECT output
+    uint8_t* data;    // MXFP8 payload [rows, K]
+    uint8_t* scales;  // MXFP8 scale bytes in `lay`
+    int64_t rows, K, ldx, ldy;
+    int lay;          // mxq_scale_layout
+};
+
+struct Block128Args {
+    const void* x;
+    uint8_t* data;
+    float* tile_scale_inv;
+    int64_t rows, K, ldx;
+};
+
+struct DequantArgs {
+    int kind;  // mxq_quant_kind
+    const uint8_t* data;
+    int64_t rows, K;
+    int fp8;   // mxq_fp8
+    const uint8_t* scales;
+    int lay;
+    const float* tile_scale_inv;
+    void* out;
+    bool out_bf16;
+};
+
+struct ExportArgs {
+    const uint8_t* scales;
+    int lay;
+    int64_t rows, K;
+    uint8_t* out;  // compact [rows, nb]
+};
+
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_rowwise(RowMode mode, Elt elt, const RowwiseArgs& a, cudaStream_t s);
+cudaError_t launch_block128(Elt elt, const Block128Args& a, cudaStream_t s);
+cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
+cudaError_t launch_export(const ExportArgs& a, cudaStream_t s);
+
+// Resident-grid sizing: number of SMs of the current device (cached).
+int sm_count();
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace mxq

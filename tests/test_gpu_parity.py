@@ -1,0 +1,384 @@
+"""GPU parity: every conversion of libmxq against the CPU oracle, byte for
+byte (tolerance 0: payload bytes, scale bytes and output bit patterns must
+be equal).  Small cases are compared in full, the 8192 x 8192 and MoE
+workloads on sampled rows and tiles plus properties checked over the whole
+tensor.  All calls go through the C ABI via the Python binding."""
+
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_precision_x32_gb300 as mxq
+import oracle
+from block_scaled_precision_x32_gb300 import synthetic as syn
+from tests.gpu_util import Guarded, dev_bf16, dev_f32, dev_input, host_bits, oracle_bits
+
+pytestmark = pytest.mark.gpu
+
+LAYOUTS = (oracle.COMPACT, oracle.PADDED, oracle.SWIZZLED)
+
+
+@pytest.fixture(scope="module")
+def mx():
+    return mxq.library()
+
+
+def _rows_k(a):
+    K = a.shape[-1]
+    return (a.size // K if K else 0), K
+
+
+def run_all_and_compare(mx, x_np, layouts=LAYOUTS, block128=True, guard=True):
+    """Projection, MXFP8 row (every layout), 128x128 blockwise, export and
+    dequantize of one input, each against the oracle."""
+    x = dev_input(x_np)
+    rows, K = _rows_k(x_np)
+    dtype = x.dtype
+
+    # projection
+    y = Guarded(x.shape, dtype) if guard else None
+    got = mx.fake_quant_mxfp4(x, out=y.t if y else None)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host_bits(got), oracle_bits(oracle.fake_quant_mxfp4(x_np)))
+    if y:
+        assert y.intact()
+
+    # MXFP8 rowwise, each scale layout, then export and dequantize
+    ref_data, ref_compact = oracle.mxfp8_row_direct(x_np, oracle.COMPACT)
+    for lay in layouts:
+        nbytes = mx.scale_bytes(rows, K, lay)
+        d = Guarded(x.shape, torch.uint8)
+        s = Guarded((max(nbytes, 1),), torch.uint8)
+        mx.mxfp8_row_direct(x, lay, data=d.t, scales=s.t)
+        torch.cuda.synchronize()
+        assert d.intact() and s.intact()
+        np.testing.assert_array_equal(host_bits(d.t), ref_data)
+        ref_lay = ref_compact.reshape(-1) if lay == oracle.COMPACT else oracle.scales_to_layout(ref_compact, rows, K, lay)
+        np.testing.assert_array_equal(host_bits(s.t)[:nbytes], ref_lay)
+        for kind in ("e4m3", "e5m2"):
+            comp = mx.export_mxfp8(d.t, s.t[:nbytes], shape=x.shape, layout=lay, fp8=kind)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(host_bits(comp.scale_inv).reshape(rows, -1), ref_compact.reshape(rows, -1))
+            assert comp.data.dtype == (torch.float8_e4m3fn if kind == "e4m3" else torch.float8_e5m2)
+            assert comp.data.data_ptr() == d.t.data_ptr()
+            nb = (K + 31) // 32
+            assert comp.is_view == (lay == oracle.COMPACT or (lay == oracle.PADDED and nb % 4 == 0))
+            for odt, ocode in ((torch.float32, oracle.FP32), (torch.bfloat16, oracle.BF16)):
+                ok = oracle.E4M3 if kind == "e4m3" else oracle.E5M2
+                want = oracle_bits(oracle.dequant_mxfp8(ref_data, ref_compact, oracle.COMPACT, ok, ocode))
+                a = mx.dequantize(d.t, scales=s.t[:nbytes], layout=lay, fp8=kind, out_dtype=odt)
+                b = mx.dequantize(comp.data.view(torch.uint8), scales=comp.scale_inv.contiguous(), layout="compact",
+                                  fp8=kind, out_dtype=odt)
+                torch.cuda.synchronize()
+                np.testing.assert_array_equal(host_bits(a), want)
+                np.testing.assert_array_equal(host_bits(b), want)  # export decodes to dequantize()
+
+    if block128:
+        ref_d, ref_s = oracle.fp8_block128_direct(x_np)
+        d = Guarded(x.shape, torch.uint8)
+        s = Guarded((max(mx.tile_scale_count(rows, K), 1),), torch.float32)
+        mx.fp8_block128_direct(x, data=d.t, tile_scale_inv=s.t)
+        torch.cuda.synchronize()
+        assert d.intact() and s.intact()
+        np.testing.assert_array_equal(host_bits(d.t), ref_d)
+        np.testing.assert_array_equal(host_bits(s.t)[:ref_s.size], ref_s.view(np.uint32).reshape(-1))
+        for odt, ocode in ((torch.float32, oracle.FP32), (torch.bfloat16, oracle.BF16)):
+            got = mx.dequantize(d.t, tile_scale_inv=s.t, out_dtype=odt)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(host_bits(got), oracle_bits(oracle.dequant_block128(ref_d, ref_s, ocode)))
+
+
+# ------------------------------------------------ exhaustive bf16 corpus
+
+def test_exhaustive_bf16_corpus(mx):
+    """All 65536 bf16 patterns, one block per row: projection, MXFP8 rowwise,
+    export, dequantize and (with partial 32-column tiles) blockwise."""
+    run_all_and_compare(mx, syn.exhaustive_bf16())
+
+
+# ------------------------------------------------ partial-block fp32 set
+
+@pytest.mark.parametrize("shape", syn.PARTIAL_BLOCK_SHAPES)
+def test_partial_block_fp32(mx, shape):
+    run_all_and_compare(mx, syn.partial_block_fp32(shape))
+
+
+# ---------------------------------------------------------- edge shapes
+
+@pytest.mark.parametrize("shape", [(1, 1), (1, 17), (3, 33), (129, 130), (2, 16), (5, 48), (257, 264), (130, 7184)])
+@pytest.mark.parametrize("dt", ["bf16", "fp32"])
+def test_edge_shapes(mx, shape, dt):
+    g = np.random.default_rng(zlib.crc32(repr((shape, dt)).encode()))
+    w = (g.standard_normal(shape) * np.ldexp(1.0, g.integers(-30, 30, size=(shape[0], 1)))).astype(np.float32)
+    x = syn.f32_to_bf16_bits(w) if dt == "bf16" else w
+    run_all_and_compare(mx, x)
+
+
+def test_fp32_random_bit_patterns(mx):
+    """Finite fp32 bit patterns over every exponent range, with Inf/NaN
+    planted in a few blocks (non-finite block poisoning)."""
+    g = np.random.default_rng(21)
+    u = g.integers(0, 0x7F800000, size=(384, 160), dtype=np.uint64).astype(np.uint32)
+    for r in range(0, 384, 2):  # rows of one binade band, so scales span 2^-126..2^125
+        e = int(g.integers(1, 255))
+        u[r] = (np.uint32(e) << np.uint32(23)) | (u[r] & np.uint32(0x7FFFFF))
+    u |= g.integers(0, 2, size=u.shape).astype(np.uint32) << np.uint32(31)
+    u[3, 5] = 0x7F800000
+    u[40, 100] = 0xFF800000
+    u[77, 0] = 0x7FC00001
+    u[200, 159] = 0xFFFFFFFF
+    run_all_and_compare(mx, u.view(np.float32))
+
+
+def test_bf16_edge_values(mx):
+    """Ladder 2^-127..2^-133, the 2^-128 tie, 1.5*2^k +-1 ulp, saturation
+    past 6*2^125 and signed zeros (TE PR #3264, "Test results (B200)")."""
+    rows = []
+    for k in range(-133, -126):
+        r = np.zeros(32, dtype=np.uint16)
+        r[3] = syn.f32_to_bf16_bits(np.array([np.ldexp(1.0, k)], dtype=np.float32))[0]
+        r[4] = r[3] | 0x8000
+        rows.append(r)
+    for k in range(-120, 128, 7):
+        c = int(syn.f32_to_bf16_bits(np.array([1.5 * 2.0 ** k], dtype=np.float32))[0])
+        r = np.zeros(32, dtype=np.uint16)
+        r[:3] = [c - 1, c, c + 1]
+        r[3:6] = [c - 0x40, c - 0x3F, c - 0x41]
+        rows.append(r)
+    sat = np.arange(0x7F38, 0x7F80, dtype=np.uint16)[:32]
+    rows.append(sat)
+    rows.append(sat | 0x8000)
+    rows.append(np.array([0x8000] * 16 + [0] * 16, dtype=np.uint16))
+    run_all_and_compare(mx, np.stack(rows))
+
+
+# -------------------------------------------------- views and in place
+
+@pytest.mark.parametrize("dt", ["bf16", "fp32"])
+def test_misaligned_and_strided_views(mx, dt):
+    """Views that start one element late and rows with padding take the
+    scalar path and give the same bytes (TE PR #3264: misaligned views)."""
+    g = np.random.default_rng(5)
+    rows, K = 67, 200
+    w = (g.standard_normal((rows, K + 9)) * 0.02).astype(np.float32)
+    base = dev_bf16(syn.f32_to_bf16_bits(w)) if dt == "bf16" else dev_f32(w)
+    for view in (base[:, 1:K + 1], base[:, :K], base[:, 3:3 + 64]):
+        x_np = host_bits(view.contiguous())
+        x_np = x_np if dt == "bf16" else x_np.view(np.float32)
+        np.testing.assert_array_equal(host_bits(mx.fake_quant_mxfp4(view)), oracle_bits(oracle.fake_quant_mxfp4(x_np)))
+        d, s = mx.mxfp8_row_direct(view, "compact")
+        rd, rs = oracle.mxfp8_row_direct(x_np)
+        np.testing.assert_array_equal(host_bits(d), rd)
+        np.testing.assert_array_equal(host_bits(s), rs)
+        d, s = mx.fp8_block128_direct(view)
+        rd, rs = oracle.fp8_block128_direct(x_np)
+        np.testing.assert_array_equal(host_bits(d), rd)
+        np.testing.assert_array_equal(host_bits(s), rs.view(np.uint32))
+
+
+def test_in_place_projection(mx):
+    x_np = syn.partial_block_fp32((128, 96))
+    x = dev_f32(x_np)
+    out = mx.fake_quant_mxfp4(x, out=x)
+    assert out.data_ptr() == x.data_ptr()
+    np.testing.assert_array_equal(host_bits(x), oracle_bits(oracle.fake_quant_mxfp4(x_np)))
+
+
+def test_fp16_and_cpu_rejected(mx):
+    with pytest.raises(mxq.MXQError) as ei:
+        mx.fake_quant_mxfp4(torch.zeros(4, 32, dtype=torch.float16, device="cuda"))
+    assert ei.value.status == 2
+    with pytest.raises(mxq.MXQError):
+        mx.dequantize(torch.zeros(4, 32, dtype=torch.uint8, device="cuda"),
+                      scales=torch.zeros(4, 1, dtype=torch.uint8, device="cuda"),
+                      out=torch.empty(4, 32, dtype=torch.float16, device="cuda"))
+    with pytest.raises(ValueError):
+        mx.fake_quant_mxfp4(torch.zeros(4, 32, dtype=torch.bfloat16))
+
+
+def test_empty_tensors(mx):
+    for shape in ((0, 32), (4, 0), (0, 0)):
+        x = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+        assert mx.fake_quant_mxfp4(x).shape == shape
+        d, s = mx.mxfp8_row_direct(x, "swizzled")
+        assert d.shape == shape
+        c = mx.export_mxfp8(d, s, shape=shape, layout="swizzled")
+        assert c.scale_inv.shape == (shape[0], (shape[1] + 31) // 32)
+
+
+def test_export_without_rowwise_data(mx):
+    with pytest.raises(mxq.MXQError) as ei:
+        mx.export_mxfp8(None, torch.zeros(128, 4, dtype=torch.uint8, device="cuda"), shape=(100, 48),
+                        layout="padded")
+    assert ei.value.status == 3
+
+
+# ----------------------------------------------------- dequantize alone
+
+@pytest.mark.parametrize("lay", LAYOUTS)
+@pytest.mark.parametrize("kind", [oracle.E4M3, oracle.E5M2])
+def test_dequant_every_payload_and_scale_code(mx, lay, kind):
+    """Every payload byte against every 16th scale code plus codes 0, 1,
+    127, 254 and 255 (TE PR #3264: planted extreme scale codes)."""
+    codes = sorted(set(range(0, 256, 16)) | {0, 1, 127, 254, 255})
+    rows, K = len(codes) * 4, 256 + 16
+    g = np.random.default_rng(kind * 10 + lay)
+    data = np.tile(np.arange(256, dtype=np.uint8), (rows, 2))[:, :K].copy()
+    g.shuffle(data, axis=1)
+    nb = (K + 31) // 32
+    compact = np.repeat(np.array(codes, dtype=np.uint8), 4)[:, None].repeat(nb, axis=1)
+    compact[:, 1] = g.integers(0, 256, size=rows, dtype=np.uint8)
+    scales = compact.reshape(-1) if lay == oracle.COMPACT else oracle.scales_to_layout(compact, rows, K, lay)
+    d = torch.from_numpy(data).cuda()
+    s = torch.from_numpy(scales).cuda()
+    for odt, ocode in ((torch.float32, oracle.FP32), (torch.bfloat16, oracle.BF16)):
+        got = mx.dequantize(d, scales=s, layout=lay, fp8="e4m3" if kind == oracle.E4M3 else "e5m2", out_dtype=odt)
+        np.testing.assert_array_equal(host_bits(got), oracle_bits(oracle.dequant_mxfp8(data, compact, oracle.COMPACT, kind, ocode)))
+
+
+def test_dequant_block128_arbitrary_scales(mx):
+    """Blockwise dequantize with scale_inv that are not powers of two
+    (rounded fp32 products, subnormal results, overflow to Inf)."""
+    g = np.random.default_rng(3)
+    rows, K = 300, 400
+    data = g.integers(0, 256, size=(rows, K), dtype=np.uint8)
+    tiles = ((rows + 127) // 128, (K + 127) // 128)
+    sinv = (g.standard_normal(tiles) * np.ldexp(1.0, g.integers(-140, 120, size=tiles))).astype(np.float32)
+    sinv[0, 0] = np.float32(3.4e38)
+    sinv[0, 1] = np.float32(1e-44)
+    d = torch.from_numpy(data).cuda()
+    s = torch.from_numpy(sinv).cuda()
+    for odt, ocode in ((torch.float32, oracle.FP32), (torch.bfloat16, oracle.BF16)):
+        got = mx.dequantize(d, tile_scale_inv=s, out_dtype=odt)
+        np.testing.assert_array_equal(host_bits(got), oracle_bits(oracle.dequant_block128(data, sinv, ocode)))
+
+
+# ------------------------------------------- full-size workloads, sampled
+
+def _sample_rows(rows, n, seed):
+    g = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, rows - 1], g.integers(0, rows, size=n)]))
+
+
+def test_large_bf16_8192_sampled(mx):
+    """8192 x 8192 bf16 N(0, 0.02): every conversion at full size in the
+    configuration the benchmark times; sampled rows and tile bands against
+    the oracle, decode properties over the whole tensor."""
+    x_np = syn.normal_bf16(8192, 8192)
+    x = dev_bf16(x_np)
+    y = mx.fake_quant_mxfp4(x)
+    d, s = mx.mxfp8_row_direct(x, "swizzled")
+    comp = mx.export_mxfp8(d, s, shape=x.shape, layout="swizzled")
+    bd, bs = mx.fp8_block128_direct(x)
+    dq = mx.dequantize(d, scales=s, layout="swizzled", out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    # properties over the whole tensor: row decode == projection (bit for bit),
+    # blockwise decode == projection when the tile spread allows (N(0, .02) spreads stay small)
+    assert torch.equal(dq.view(torch.int16), y.view(torch.int16))
+    bq = mx.dequantize(bd, tile_scale_inv=bs, out_dtype=torch.float32)
+    assert torch.equal(bq.view(torch.int32), y.float().view(torch.int32))
+    rows = _sample_rows(8192, 40, 1)
+    ref_y = oracle.fake_quant_mxfp4(x_np[rows])
+    np.testing.assert_array_equal(host_bits(y[rows]), ref_y)
+    rd, rs = oracle.mxfp8_row_direct(x_np[rows])
+    np.testing.assert_array_equal(host_bits(d[rows]), rd)
+    np.testing.assert_array_equal(host_bits(comp.scale_inv[rows]), rs)
+    for band in (0, 31, 63):
+        sl = slice(band * 128, band * 128 + 128)
+        rd, rs = oracle.fp8_block128_direct(x_np[sl])
+        np.testing.assert_array_equal(host_bits(bd[sl]), rd)
+        np.testing.assert_array_equal(host_bits(bs[band]), rs.view(np.uint32)[0])
+
+
+def _tile_spread(x_np):
+    """Spread of the 1x32 block exponents (finite, nonzero blocks) per 128x128 tile."""
+    rows, K = x_np.shape
+    a = np.abs(x_np.astype(np.float64)).reshape(rows, K // 32, 32).max(axis=2)
+    with np.errstate(divide="ignore"):
+        e = np.ceil(np.log2(a / 6.0))
+    e = np.clip(e, -126, 125)
+    e[a == 0] = np.nan
+    e = e.reshape(rows // 128, 128, K // 128, 4).transpose(0, 2, 1, 3).reshape(rows // 128, K // 128, -1)
+    with np.errstate(invalid="ignore"):
+        return np.nanmax(e, axis=2) - np.nanmin(e, axis=2)
+
+
+def test_spread_sweep_fp32_8192(mx):
+    """128x128 tiles of E2M1 payloads with block exponents spread by d in
+    0..16: the blockwise decode equals the projection through spread 14
+    (TE PR #3264, "Test results (B200)"); sampled bands against the oracle."""
+    x_np, _ = syn.spread_tiles_fp32()
+    x = dev_f32(x_np)
+    bd, bs = mx.fp8_block128_direct(x)
+    y = mx.fake_quant_mxfp4(x)
+    bq = mx.dequantize(bd, tile_scale_inv=bs, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    eq = (bq.view(torch.int32) == y.view(torch.int32)).view(64, 128, 64, 128).all(dim=3).all(dim=1).cpu().numpy()
+    spread = _tile_spread(x_np)
+    with np.errstate(invalid="ignore"):
+        assert eq[spread <= 14].all()
+        assert (~eq[spread >= 15]).any()
+    for band in (0, 17, 63):
+        sl = slice(band * 128, band * 128 + 128)
+        rd, rs = oracle.fp8_block128_direct(x_np[sl])
+        np.testing.assert_array_equal(host_bits(bd[sl]), rd)
+        np.testing.assert_array_equal(host_bits(bs[band]), rs.view(np.uint32)[0])
+
+
+def test_moe_expert_stack_export(mx):
+    """32 experts x 4096 x 7184 bf16 (K % 32 = 16, 225 scale columns):
+    MXFP8 rowwise into the GEMM-swizzled layout, then export; sampled
+    experts against the oracle, swizzle invariance over the whole stack."""
+    E, R, K = syn.MOE_EXPERTS, syn.MOE_ROWS, syn.MOE_K
+    x = torch.empty((E, R, K), dtype=torch.bfloat16, device="cuda")
+    host = {}
+    for e in range(E):
+        xe = syn.moe_expert_bf16(e)
+        if e in (0, 13, 31):
+            host[e] = xe
+        x[e].copy_(dev_bf16(xe))
+    d, s = mx.mxfp8_row_direct(x, "swizzled")
+    comp = mx.export_mxfp8(d, s, shape=x.shape, layout="swizzled")
+    _, s_compact = mx.mxfp8_row_direct(x, "compact")
+    torch.cuda.synchronize()
+    assert comp.scale_inv.shape == (E, R, 225) and not comp.is_view
+    assert torch.equal(comp.scale_inv, s_compact)
+    # padding columns 225..227 of the swizzled buffer are zero
+    r = torch.arange(E * R, device="cuda", dtype=torch.int64)[:, None]
+    j = torch.tensor([225, 226, 227], device="cuda", dtype=torch.int64)[None, :]
+    off = ((r // 128) * 57 + j // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + j % 4
+    assert int(s.view(-1)[off.view(-1)].max()) == 0
+    for e, xe in host.items():
+        rows = _sample_rows(R, 12, e)
+        rd, rs = oracle.mxfp8_row_direct(xe[rows])
+        np.testing.assert_array_equal(host_bits(d[e][rows]), rd)
+        np.testing.assert_array_equal(host_bits(comp.scale_inv[e][rows]), rs)
+
+
+# ------------------------------------------------------- fast-math build
+
+def test_fast_math_build_gives_identical_bytes(mx):
+    """The same sources built with --use_fast_math give identical bytes
+    (TE PR #3264, "Test results (B200)")."""
+    fm = mxq.Library(fastmath=True)
+    g = np.random.default_rng(8)
+    u = g.integers(0, 0x7F800000, size=(256, 128), dtype=np.uint64).astype(np.uint32)
+    u[::2] = (u[::2] & 0x807FFFFF) | (np.uint32(3) << np.uint32(23))  # subnormal-scale rows
+    inputs = [syn.exhaustive_bf16(), u.view(np.float32), syn.spread_tiles_fp32(rows=256, K=512)[0]]
+    for x_np in inputs:
+        x = dev_input(x_np)
+        for lib_a, lib_b in ((mx, fm),):
+            assert torch.equal(lib_a.fake_quant_mxfp4(x).view(torch.uint8), lib_b.fake_quant_mxfp4(x).view(torch.uint8))
+            for lay in ("compact", "swizzled"):
+                da, sa = lib_a.mxfp8_row_direct(x, lay)
+                db, sb = lib_b.mxfp8_row_direct(x, lay)
+                assert torch.equal(da, db) and torch.equal(sa, sb)
+                for odt in (torch.float32, torch.bfloat16):
+                    qa = lib_a.dequantize(da, scales=sa, layout=lay, out_dtype=odt)
+                    qb = lib_b.dequantize(db, scales=sb, layout=lay, out_dtype=odt)
+                    assert torch.equal(qa.view(torch.uint8), qb.view(torch.uint8))
+            da, sa = lib_a.fp8_block128_direct(x)
+            db, sb = lib_b.fp8_block128_direct(x)
+            assert torch.equal(da, db) and torch.equal(sa.view(torch.int32), sb.view(torch.int32))
