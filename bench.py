@@ -166,53 +166,85 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
 
     names = list(BYTES)
-
-    def step(s, ev=None):
-        k = 3 * s
-        calls = [
-            lambda: lib.fake_quant_mxfp4(xs[k % R], out=y),
-            lambda: lib.mxfp8_row_direct(xs[(k + 1) % R], "swizzled", data=row_d, scales=row_s),
-            lambda: lib.fp8_block128_direct(xs[(k + 2) % R], data=blk_d, tile_scale_inv=blk_s),
-            lambda: lib.dequantize(dq_in[s % R][0], scales=dq_in[s % R][1], layout="swizzled", out=dq_out),
-            lambda: lib.export_mxfp8(dq_in[s % R][0], dq_in[s % R][1], shape=(ROWS, COLS), layout="swizzled",
-                                     scale_out=ex_out),
-        ]
-        for i, c in enumerate(calls):
-            if ev is not None:
-                ev[i][0].record(stream)
-            c()
-            if ev is not None:
-                ev[i][1].record(stream)
-
-    for s in range(args.warmup):
-        step(s)
+    # Prepared calls (arguments marshalled once), made on a side stream and
+    # captured into CUDA graphs: one graph per input rotation holding the
+    # step's five launches, and per conversion one graph of R back-to-back
+    # launches.  Replays leave the host out of the timed loop.
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        plans = []
+        for s in range(R):
+            k = 3 * s
+            dq_d, dq_s = dq_in[s]
+            plans.append([
+                lib.plan_fake_quant_mxfp4(xs[k % R], y),
+                lib.plan_mxfp8_row_direct(xs[(k + 1) % R], "swizzled", row_d, row_s),
+                lib.plan_fp8_block128_direct(xs[(k + 2) % R], blk_d, blk_s),
+                lib.plan_dequantize(dq_d, dq_out, scales=dq_s, layout="swizzled"),
+                lib.plan_export_mxfp8(dq_d, dq_s, shape=(ROWS, COLS), layout="swizzled", scale_out=ex_out)[0],
+            ])
+        for s in range(2 * R):  # warm every launch configuration before capture
+            for c in plans[s % R]:
+                c()
+        side.synchronize()
+        step_graphs, conv_graphs = [], []
+        for s in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for c in plans[s]:
+                    c()
+            step_graphs.append(g)
+        for i in range(len(names)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for s in range(R):
+                    plans[s][i]()
+            conv_graphs.append(g)
+    torch.cuda.current_stream(dev).wait_stream(side)
     torch.cuda.synchronize()
 
-    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in names]
-           for _ in range(args.steps)]
+    for s in range(args.warmup):
+        step_graphs[s % R].replay()
+    torch.cuda.synchronize()
+
+    # timed region 1: exactly `steps` steps
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     with Clocks(dev.index) as clk:
         t0.record(stream)
         for s in range(args.steps):
-            step(args.warmup + s, evs[s])
+            step_graphs[s % R].replay()
         t1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
     elapsed_ms = t0.elapsed_time(t1)
-    per = {nm: [evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)] for i, nm in enumerate(names)}
     ms_step = max_over_ranks(elapsed_ms, world) / args.steps
 
+    # timed region 2: each conversion alone, R * ceil(steps / R) launches back to back
+    reps = max(1, -(-args.steps // R))
+    per = {}
+    for i, nm in enumerate(names):
+        conv_graphs[i].replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            conv_graphs[i].replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        per[nm] = max_over_ranks(a.elapsed_time(b), world) / (reps * R)
+
     # end to end through the public API: pinned host weight in, every result back to pinned host memory
-    e2e = run_e2e(args, lib, dev, x_host, world)
+    e2e = None if args.no_e2e else run_e2e(args, lib, dev, x_host, world)
 
     if rank != 0:
         return None
     peak, peak_src = load_peaks()
     per_conv = {}
     for nm in names:
-        us = statistics.mean(per[nm]) * 1e3
+        us = per[nm] * 1e3
         gbs = BYTES[nm] / (us * 1e-6) / 1e9
         per_conv[nm] = {"us": round(us, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
                         "bytes": BYTES[nm]}
@@ -235,50 +267,104 @@ def run_gpu(args, rank, world):
         "clocks": clk.result,
         "e2e": e2e,
         "gpu_launches": len(names) * args.steps,
+        "timing": "CUDA events on the launch stream; steps replay one CUDA graph per input rotation (5 launches "
+                  "each); per_conversion replays per-kernel graphs of back-to-back launches",
     }
 
 
-def run_e2e(args, lib, dev, x_host, world):
+def run_e2e(args, lib, dev, x_host, world, chunks: int = 8):
+    """The same five conversions through the public API with the weight in
+    pinned host memory and every result copied back to pinned host memory.
+    The weight is cut into row chunks (multiples of 128 rows, so every
+    scale layout splits into contiguous slices); chunk c's upload, its five
+    conversions and its downloads run on three streams, so copies overlap
+    the kernels of neighbouring chunks."""
     import torch
 
+    rows_c = ROWS // chunks
+    nbc = NB
     xh = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
-    outs = {
+    host = {
         "y": torch.empty(xh.shape, dtype=torch.bfloat16).pin_memory(),
         "row_d": torch.empty(xh.shape, dtype=torch.uint8).pin_memory(),
         "row_s": torch.empty(lib.scale_bytes(ROWS, COLS, "swizzled"), dtype=torch.uint8).pin_memory(),
         "blk_d": torch.empty(xh.shape, dtype=torch.uint8).pin_memory(),
         "blk_s": torch.empty(lib.tile_scale_count(ROWS, COLS), dtype=torch.float32).pin_memory(),
         "dq": torch.empty(xh.shape, dtype=torch.bfloat16).pin_memory(),
-        "ex": torch.empty(ROWS * NB, dtype=torch.uint8).pin_memory(),
+        "ex": torch.empty(ROWS * nbc, dtype=torch.uint8).pin_memory(),
     }
-    stream = torch.cuda.current_stream(dev)
+    devb = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in host.items()}
+    xd = torch.empty(xh.shape, dtype=torch.bfloat16, device=dev)
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def sl(name, c):  # chunk c of a buffer (every layout splits by 128-row bands)
+        t = devb[name] if name != "x" else xd
+        h = host[name] if name != "x" else xh
+        if name in ("row_s",):
+            n = lib.scale_bytes(rows_c, COLS, "swizzled")
+            return t[c * n:(c + 1) * n], h[c * n:(c + 1) * n]
+        if name == "blk_s":
+            n = lib.tile_scale_count(rows_c, COLS)
+            return t[c * n:(c + 1) * n], h[c * n:(c + 1) * n]
+        if name == "ex":
+            n = rows_c * nbc
+            return t[c * n:(c + 1) * n], h[c * n:(c + 1) * n]
+        return t[c * rows_c:(c + 1) * rows_c], h[c * rows_c:(c + 1) * rows_c]
+
+    plans = []
+    with torch.cuda.stream(s_cmp):
+        for c in range(chunks):
+            x_c, _ = sl("x", c)
+            y_c, rd_c, rs_c = sl("y", c)[0], sl("row_d", c)[0], sl("row_s", c)[0]
+            bd_c, bs_c, dq_c, ex_c = sl("blk_d", c)[0], sl("blk_s", c)[0], sl("dq", c)[0], sl("ex", c)[0]
+            plans.append([
+                lib.plan_fake_quant_mxfp4(x_c, y_c),
+                lib.plan_mxfp8_row_direct(x_c, "swizzled", rd_c, rs_c),
+                lib.plan_fp8_block128_direct(x_c, bd_c, bs_c),
+                lib.plan_dequantize(rd_c, dq_c, scales=rs_c, layout="swizzled"),
+                lib.plan_export_mxfp8(rd_c, rs_c, shape=(rows_c, COLS), layout="swizzled", scale_out=ex_c)[0],
+            ])
+    ev_in = [torch.cuda.Event() for _ in range(chunks)]
+    ev_cmp = [torch.cuda.Event() for _ in range(chunks)]
 
     def step():
-        x = xh.to(dev, non_blocking=True)
-        y = lib.fake_quant_mxfp4(x)
-        d, s = lib.mxfp8_row_direct(x, "swizzled")
-        bd, bs = lib.fp8_block128_direct(x)
-        dq = lib.dequantize(d, scales=s, layout="swizzled")
-        comp = lib.export_mxfp8(d, s, shape=(ROWS, COLS), layout="swizzled")
-        for k, t in (("y", y), ("row_d", d), ("row_s", s), ("blk_d", bd), ("blk_s", bs), ("dq", dq),
-                     ("ex", comp.scale_inv.reshape(-1))):
-            outs[k].copy_(t.reshape(outs[k].shape), non_blocking=True)
+        for c in range(chunks):
+            with torch.cuda.stream(s_in):
+                d, h = sl("x", c)
+                d.copy_(h, non_blocking=True)
+                ev_in[c].record(s_in)
+            s_cmp.wait_event(ev_in[c])
+            for call in plans[c]:
+                call()
+            ev_cmp[c].record(s_cmp)
+            s_out.wait_event(ev_cmp[c])
+            with torch.cuda.stream(s_out):
+                for name in host:
+                    d, h = sl(name, c)
+                    h.copy_(d, non_blocking=True)
 
+    main = torch.cuda.current_stream(dev)
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize()
     n = max(1, min(args.steps, 10))
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    t0.record(stream)
+    torch.cuda.synchronize()
+    t0.record(main)
+    for st in (s_in, s_cmp, s_out):
+        st.wait_event(t0)
     for _ in range(n):
         step()
-    t1.record(stream)
+    for st in (s_in, s_cmp, s_out):
+        main.wait_stream(st)
+    t1.record(main)
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world) / n
-    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    d2h = sum(t.numel() * t.element_size() for t in host.values())
     return {"value": round(world * STEP_BYTES / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 3),
-            "h2d_bytes_per_step": int(xh.numel() * 2), "d2h_bytes_per_step": int(d2h), "steps": n}
+            "h2d_bytes_per_step": int(xh.numel() * 2), "d2h_bytes_per_step": int(d2h), "steps": n,
+            "pipeline": f"{chunks} row chunks over 3 streams (upload / convert / download)"}
 
 
 # --------------------------------------------------- CPU oracle (reference)
@@ -383,10 +469,11 @@ def max_over_ranks(v: float, world: int) -> float:
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["mxq", "reference"], default="mxq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -26,7 +26,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "MXQError", "MXFP8Components", "Library", "library",
+    "MXQError", "MXFP8Components", "Library", "Call", "library",
     "mxq_fake_quant_mxfp4", "mxq_mxfp8_row_direct", "mxq_fp8_block128_direct",
     "mxq_dequantize", "mxq_export_mxfp8", "mxq_scale_bytes", "mxq_tile_scale_count",
     "COMPACT", "PADDED", "SWIZZLED", "scale_cols",
@@ -166,78 +166,58 @@ class Library:
     def tile_scale_count(self, rows: int, K: int) -> int:
         return int(self.L.mxq_tile_scale_count(rows, K))
 
-    # -- conversions ----------------------------------------------------
-    def fake_quant_mxfp4(self, x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    # -- prepared calls -------------------------------------------------
+    # Each plan_* validates and marshals its arguments once and returns a
+    # Call: invoking it enqueues the one kernel on the stream that was
+    # current when the plan was made.  The Call keeps its tensors alive.
+    # The eager methods below are plan_*(...)() with freshly allocated
+    # outputs.
+
+    def plan_fake_quant_mxfp4(self, x: torch.Tensor, out: torch.Tensor) -> "Call":
         _need_cuda(x, out)
         dt = _dt_code(x)
         rows, K, ldx = _rows_view(x)
-        if out is None:
-            out = torch.empty_like(x, memory_format=torch.contiguous_format)
         if out.shape != x.shape or out.dtype != x.dtype:
             raise ValueError("out must match x in shape and dtype")
         _, _, ldy = _rows_view(out)
-        with torch.cuda.device(x.device):
-            self._check(self.L.mxq_fake_quant_mxfp4(x.data_ptr(), out.data_ptr(), dt, rows, K, ldx, ldy,
-                                                    _stream(x)), "mxq_fake_quant_mxfp4")
-        return out
+        args = (ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(out.data_ptr()), dt, rows, K, ldx, ldy, _stream(x))
+        return Call(self, self.L.mxq_fake_quant_mxfp4, args, "mxq_fake_quant_mxfp4", (x, out), x.device)
 
-    def mxfp8_row_direct(self, x: torch.Tensor, layout="compact", data: Optional[torch.Tensor] = None,
-                         scales: Optional[torch.Tensor] = None):
-        """Returns (payload uint8 of x's shape, scales).  Compact scales are
-        shaped (*shape[:-1], nb); padded and swizzled ones (Rp, Cp)."""
+    def plan_mxfp8_row_direct(self, x: torch.Tensor, layout, data: torch.Tensor, scales: torch.Tensor) -> "Call":
         _need_cuda(x, data, scales)
         dt = _dt_code(x)
         lay = _LAYOUTS[layout]
         rows, K, ldx = _rows_view(x)
-        nb = scale_cols(K)
-        if data is None:
-            data = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
-        if scales is None:
-            if lay == COMPACT:
-                scales = torch.empty(tuple(x.shape[:-1]) + (nb,), dtype=torch.uint8, device=x.device)
-            else:
-                scales = torch.empty(((rows + 127) // 128 * 128, (nb + 3) // 4 * 4), dtype=torch.uint8,
-                                     device=x.device)
         if not data.is_contiguous() or data.numel() != rows * K or data.dtype != torch.uint8:
             raise ValueError("data must be a contiguous uint8 tensor of rows*K bytes")
-        if not scales.is_contiguous() or scales.numel() < self.scale_bytes(rows, K, lay):
-            raise ValueError("scales buffer too small or not contiguous")
-        with torch.cuda.device(x.device):
-            self._check(self.L.mxq_mxfp8_row_direct(x.data_ptr(), dt, rows, K, ldx, data.data_ptr(),
-                                                    scales.data_ptr(), lay, _stream(x)), "mxq_mxfp8_row_direct")
-        return data, scales
+        if not scales.is_contiguous() or scales.dtype != torch.uint8 or scales.numel() < self.scale_bytes(rows, K, lay):
+            raise ValueError("scales must be a contiguous uint8 buffer of mxq_scale_bytes() bytes")
+        args = (ctypes.c_void_p(x.data_ptr()), dt, rows, K, ldx, ctypes.c_void_p(data.data_ptr()),
+                ctypes.c_void_p(scales.data_ptr()), lay, _stream(x))
+        return Call(self, self.L.mxq_mxfp8_row_direct, args, "mxq_mxfp8_row_direct", (x, data, scales), x.device)
 
-    def fp8_block128_direct(self, x: torch.Tensor, data: Optional[torch.Tensor] = None,
-                            tile_scale_inv: Optional[torch.Tensor] = None):
-        """Returns (E4M3 payload uint8 of x's shape, fp32 2^T per 128x128 tile)."""
+    def plan_fp8_block128_direct(self, x: torch.Tensor, data: torch.Tensor, tile_scale_inv: torch.Tensor) -> "Call":
         _need_cuda(x, data, tile_scale_inv)
         dt = _dt_code(x)
         rows, K, ldx = _rows_view(x)
-        if data is None:
-            data = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
-        if tile_scale_inv is None:
-            tile_scale_inv = torch.empty(((rows + 127) // 128, (K + 127) // 128), dtype=torch.float32,
-                                         device=x.device)
-        if not data.is_contiguous() or data.numel() != rows * K:
+        if not data.is_contiguous() or data.numel() != rows * K or data.dtype != torch.uint8:
             raise ValueError("data must be a contiguous uint8 tensor of rows*K bytes")
         if tile_scale_inv.dtype != torch.float32 or tile_scale_inv.numel() < self.tile_scale_count(rows, K):
             raise ValueError("tile_scale_inv must be fp32 with ceil(rows/128)*ceil(K/128) entries")
-        with torch.cuda.device(x.device):
-            self._check(self.L.mxq_fp8_block128_direct(x.data_ptr(), dt, rows, K, ldx, data.data_ptr(),
-                                                       tile_scale_inv.data_ptr(), _stream(x)),
-                        "mxq_fp8_block128_direct")
-        return data, tile_scale_inv
+        args = (ctypes.c_void_p(x.data_ptr()), dt, rows, K, ldx, ctypes.c_void_p(data.data_ptr()),
+                ctypes.c_void_p(tile_scale_inv.data_ptr()), _stream(x))
+        return Call(self, self.L.mxq_fp8_block128_direct, args, "mxq_fp8_block128_direct",
+                    (x, data, tile_scale_inv), x.device)
 
-    def dequantize(self, data: torch.Tensor, *, scales: Optional[torch.Tensor] = None, layout="compact",
-                   fp8="e4m3", tile_scale_inv: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
-                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
-        """MXFP8 rowwise (pass ``scales``) or 128x128 blockwise (pass
-        ``tile_scale_inv``) payload -> bf16 / fp32 of data's shape."""
+    def plan_dequantize(self, data: torch.Tensor, out: torch.Tensor, *, scales: Optional[torch.Tensor] = None,
+                        layout="compact", fp8="e4m3", tile_scale_inv: Optional[torch.Tensor] = None) -> "Call":
         _need_cuda(data, scales, tile_scale_inv, out)
         if (scales is None) == (tile_scale_inv is None):
             raise ValueError("pass exactly one of scales (MXFP8 rowwise) or tile_scale_inv (128x128)")
         if not data.is_contiguous():
             raise ValueError("data must be contiguous")
+        if not out.is_contiguous() or out.shape != data.shape:
+            raise ValueError("out must be contiguous with data's shape")
         K = data.shape[-1] if data.dim() else 1
         rows = data.numel() // K if K else 0
         q = _Quantized()
@@ -248,31 +228,22 @@ class Library:
         q.lay = _LAYOUTS[layout]
         q.scales = scales.data_ptr() if scales is not None else None
         q.tile_scale_inv = tile_scale_inv.data_ptr() if tile_scale_inv is not None else None
-        if out is None:
-            out = torch.empty(data.shape, dtype=out_dtype, device=data.device)
-        if not out.is_contiguous() or out.shape != data.shape:
-            raise ValueError("out must be contiguous with data's shape")
-        if out.dtype == torch.float16:
-            odt = _FP16
-        else:
-            odt = _dt_code(out)
-        with torch.cuda.device(data.device):
-            self._check(self.L.mxq_dequantize(ctypes.byref(q), out.data_ptr(), odt, _stream(data)),
-                        "mxq_dequantize")
-        return out
+        odt = _FP16 if out.dtype == torch.float16 else _dt_code(out)
+        args = (ctypes.byref(q), ctypes.c_void_p(out.data_ptr()), odt, _stream(data))
+        return Call(self, self.L.mxq_dequantize, args, "mxq_dequantize", (data, out, scales, tile_scale_inv, q),
+                    data.device)
 
-    def export_mxfp8(self, data: Optional[torch.Tensor], scales: torch.Tensor, *, shape, layout="compact",
-                     fp8="e4m3", scale_out: Optional[torch.Tensor] = None) -> MXFP8Components:
-        """export_components of an MXFP8 storage whose rowwise payload is
-        ``data`` (None = no row-scaled data) and whose scales are held in
-        ``layout``."""
+    def plan_export_mxfp8(self, data: Optional[torch.Tensor], scales: torch.Tensor, *, shape, layout="compact",
+                          fp8="e4m3", scale_out: Optional[torch.Tensor] = None):
+        """Returns (Call, MXFP8Components).  The components are views whose
+        scale bytes are valid once the Call has run (a view of the storage
+        needs no kernel; the Call then launches nothing)."""
         shape = tuple(shape)
         K = shape[-1] if shape else 0
         rows = 1
         for d in shape[:-1]:
             rows *= d
         nb = scale_cols(K)
-        dev = scales.device
         _need_cuda(scales, data, scale_out)
         st = _Storage()
         st.data = data.data_ptr() if data is not None else None
@@ -280,22 +251,93 @@ class Library:
         st.fp8 = _fp8_code(fp8)
         st.lay = _LAYOUTS[layout]
         st.rows, st.K = rows, K
-        if scale_out is None:
-            view = st.lay == COMPACT or (st.lay == PADDED and nb % 4 == 0) or rows * K == 0
-            if not view:
-                scale_out = torch.empty(rows * nb, dtype=torch.uint8, device=dev)
+        view = st.lay == COMPACT or (st.lay == PADDED and nb % 4 == 0) or rows * K == 0
+        if scale_out is None and not view:
+            scale_out = torch.empty(rows * nb, dtype=torch.uint8, device=scales.device)
         comp = _Components()
-        with torch.cuda.device(dev):
-            self._check(self.L.mxq_export_mxfp8(ctypes.byref(st), scale_out.data_ptr() if scale_out is not None else None,
-                                                scale_out.numel() if scale_out is not None else 0, ctypes.byref(comp),
-                                                _stream(scales)), "mxq_export_mxfp8")
+        args = (ctypes.byref(st), ctypes.c_void_p(scale_out.data_ptr()) if scale_out is not None else None,
+                scale_out.numel() if scale_out is not None else 0, ctypes.byref(comp), _stream(scales))
+        call = Call(self, self.L.mxq_export_mxfp8, args, "mxq_export_mxfp8", (data, scales, scale_out, st, comp),
+                    scales.device)
         fp8_dtype = torch.float8_e4m3fn if st.fp8 == _E4M3 else torch.float8_e5m2
         values = data.view(fp8_dtype).view(shape) if data is not None else None
-        if comp.is_view:
-            s = scales.reshape(-1)[: rows * nb].view(shape[:-1] + (nb,))
+        src = scales if view else scale_out
+        s = src.reshape(-1)[: rows * nb].view(shape[:-1] + (nb,))
+        return call, MXFP8Components(values, s, view)
+
+    # -- eager conversions ----------------------------------------------
+
+    def fake_quant_mxfp4(self, x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty_like(x, memory_format=torch.contiguous_format)
+        self.plan_fake_quant_mxfp4(x, out)()
+        return out
+
+    def mxfp8_row_direct(self, x: torch.Tensor, layout="compact", data: Optional[torch.Tensor] = None,
+                         scales: Optional[torch.Tensor] = None):
+        """Returns (payload uint8 of x's shape, scales).  Compact scales are
+        shaped (*shape[:-1], nb); padded and swizzled ones (Rp, Cp)."""
+        rows, K, _ = _rows_view(x)
+        nb = scale_cols(K)
+        if data is None:
+            data = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        if scales is None:
+            if _LAYOUTS[layout] == COMPACT:
+                scales = torch.empty(tuple(x.shape[:-1]) + (nb,), dtype=torch.uint8, device=x.device)
+            else:
+                scales = torch.empty(((rows + 127) // 128 * 128, (nb + 3) // 4 * 4), dtype=torch.uint8,
+                                     device=x.device)
+        self.plan_mxfp8_row_direct(x, layout, data, scales)()
+        return data, scales
+
+    def fp8_block128_direct(self, x: torch.Tensor, data: Optional[torch.Tensor] = None,
+                            tile_scale_inv: Optional[torch.Tensor] = None):
+        """Returns (E4M3 payload uint8 of x's shape, fp32 2^T per 128x128 tile)."""
+        rows, K, _ = _rows_view(x)
+        if data is None:
+            data = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        if tile_scale_inv is None:
+            tile_scale_inv = torch.empty(((rows + 127) // 128, (K + 127) // 128), dtype=torch.float32,
+                                         device=x.device)
+        self.plan_fp8_block128_direct(x, data, tile_scale_inv)()
+        return data, tile_scale_inv
+
+    def dequantize(self, data: torch.Tensor, *, scales: Optional[torch.Tensor] = None, layout="compact",
+                   fp8="e4m3", tile_scale_inv: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """MXFP8 rowwise (pass ``scales``) or 128x128 blockwise (pass
+        ``tile_scale_inv``) payload -> bf16 / fp32 of data's shape."""
+        if out is None:
+            out = torch.empty(data.shape, dtype=out_dtype, device=data.device)
+        self.plan_dequantize(data, out, scales=scales, layout=layout, fp8=fp8, tile_scale_inv=tile_scale_inv)()
+        return out
+
+    def export_mxfp8(self, data: Optional[torch.Tensor], scales: torch.Tensor, *, shape, layout="compact",
+                     fp8="e4m3", scale_out: Optional[torch.Tensor] = None) -> MXFP8Components:
+        """export_components of an MXFP8 storage whose rowwise payload is
+        ``data`` (None = no row-scaled data) and whose scales are held in
+        ``layout``."""
+        call, comp = self.plan_export_mxfp8(data, scales, shape=shape, layout=layout, fp8=fp8, scale_out=scale_out)
+        call()
+        return comp
+
+
+class Call:
+    """A prepared libmxq call (see Library.plan_*)."""
+
+    __slots__ = ("lib", "fn", "args", "name", "keep", "device")
+
+    def __init__(self, lib: "Library", fn, args, name: str, keep, device):
+        self.lib, self.fn, self.args, self.name, self.keep, self.device = lib, fn, args, name, keep, device
+
+    def __call__(self) -> None:
+        if torch.cuda.current_device() != self.device.index:
+            with torch.cuda.device(self.device):
+                status = self.fn(*self.args)
         else:
-            s = scale_out.reshape(-1)[: rows * nb].view(shape[:-1] + (nb,))
-        return MXFP8Components(values, s, bool(comp.is_view))
+            status = self.fn(*self.args)
+        if status != 0:
+            self.lib._check(status, self.name)
 
 
 _default: Optional[Library] = None

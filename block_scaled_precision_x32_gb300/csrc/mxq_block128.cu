@@ -5,11 +5,14 @@
 // T = max(max_b e_b - 6, -127) over the 1x32 blocks of a 128x128 tile, each
 // payload RTNE_E4M3(p * 2^(e_b - T)) with subnormals, no device-side assert.
 //
-// One CTA per tile, the whole tile held in registers: 256 threads x 8
-// chunks of 16 bytes (bf16) or 512 x 8 (fp32), a tile row being 16 (bf16)
-// or 32 (fp32) consecutive lanes.  Block exponents come from 4- or 8-lane
-// shuffles, the tile maximum from one redux per warp plus shared memory;
-// the tile is read from HBM exactly once.
+// One CTA per tile; the tile is read from HBM once.  A tile is 512 blocks of
+// 1x32; each lane owns whole blocks (2 per lane for bf16 with 256 threads, 1
+// for fp32 with 512), read as 32-byte vectors.  Pass 1 reads the blocks
+// (asking L1 to keep the lines) and keeps only their exponents; the tile
+// maximum is one warp redux plus a pass through shared memory; pass 2
+// re-reads the blocks -- from L1, the tile being 32 or 64 KB -- encodes
+// them and writes 32 payload bytes per block.  Holding no tile data across
+// the barrier keeps registers low and lets more tiles stream per SM.
 #include <cuda_runtime.h>
 
 #include "mxq_device.cuh"
@@ -18,84 +21,95 @@
 namespace mxq {
 namespace {
 
-constexpr int kChunks = 8;  // chunks per thread
 constexpr int kNoBlock = -100000;
 
 template <Elt ELT>
 struct T128;
 template <>
 struct T128<Elt::BF16> {
-    static constexpr int NT = 256, CPR = 16, CH = 8, ES = 2, MANT = 7, MINB = 3;
+    static constexpr int NT = 256, BPL = 2, SEGS = 2, SEG_ELEMS = 16, ES = 2, MANT = 7, MINB = 4;
 };
 template <>
 struct T128<Elt::FP32> {
-    static constexpr int NT = 512, CPR = 32, CH = 4, ES = 4, MANT = 23, MINB = 1;
+    static constexpr int NT = 512, BPL = 1, SEGS = 4, SEG_ELEMS = 8, ES = 4, MANT = 23, MINB = 2;
 };
 
-template <Elt ELT, bool VEC>
-__global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB) block128_kernel(Block128Args a, int64_t tiles_r, int64_t tiles_c) {
+// One block of the tile as SEGS x 8 words (missing elements read as +0).
+// PASS 1 reads from HBM and asks L1 to keep the lines; PASS 2 reads them
+// again (an L1 hit in the common case) and lets them go.
+template <Elt ELT, bool VEC, int PASS>
+__device__ __forceinline__ void load_blk(uint32_t (&v)[T128<ELT>::SEGS][8], const char* p, int valid) {
+    using P = T128<ELT>;
+#pragma unroll
+    for (int s = 0; s < P::SEGS; ++s) {
+        if constexpr (VEC) {
+            if (s * P::SEG_ELEMS < valid) {
+                if constexpr (PASS == 1)
+                    ld32_keep(v[s], p + 32 * s);
+                else
+                    ld32_drop(v[s], p + 32 * s);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[s][k] = 0u;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                uint32_t w = 0u;
+                if constexpr (ELT == Elt::BF16) {
+                    const int e0 = s * 16 + 2 * k;
+                    if (e0 < valid) w = reinterpret_cast<const uint16_t*>(p)[e0];
+                    if (e0 + 1 < valid) w |= (uint32_t)reinterpret_cast<const uint16_t*>(p)[e0 + 1] << 16;
+                } else {
+                    const int e0 = s * 8 + k;
+                    if (e0 < valid) w = reinterpret_cast<const uint32_t*>(p)[e0];
+                }
+                v[s][k] = w;
+            }
+        }
+    }
+}
+
+template <Elt ELT, bool VEC, int DST>
+__global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB)
+    block128_kernel(Block128Args a, int64_t tiles_r, int64_t tiles_c) {
     using P = T128<ELT>;
     __shared__ int warp_max[P::NT / 32];
     const int t = threadIdx.x;
-    const int cc = t % P::CPR;  // chunk within the tile row
     const int64_t tj = blockIdx.x;
 
     for (int64_t ti = blockIdx.y; ti < tiles_r; ti += gridDim.y) {
-        const int64_t col0 = tj * 128 + (int64_t)cc * P::CH;
-        const int64_t row0 = ti * 128 + t / P::CPR;  // this thread's rows: row0 + 16 i
-        const int64_t nvalid = col0 < a.K ? a.rows - row0 : 0;  // valid iff 16 i < nvalid
-        const char* xp = static_cast<const char*>(a.x) + (row0 * a.ldx + col0) * P::ES;
-        const int64_t xstep = 16 * a.ldx * P::ES;
-        uint4 v[kChunks];
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-            v[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (16 * i < nvalid) {
-                const char* p = xp + i * xstep;
-                if constexpr (VEC) {
-                    v[i] = __ldcs(reinterpret_cast<const uint4*>(p));
-                } else {
-                    uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                    for (int k = 0; k < P::CH; ++k) {
-                        if (col0 + k < a.K) {
-                            if constexpr (ELT == Elt::BF16)
-                                w[k >> 1] |= (uint32_t)reinterpret_cast<const uint16_t*>(p)[k] << ((k & 1) * 16);
-                            else
-                                w[k] = reinterpret_cast<const uint32_t*>(p)[k];
-                        }
-                    }
-                    v[i] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-        }
-
-        // block exponents (one byte each, 0xFF = poisoned) and the tile
-        // maximum over finite blocks
-        uint32_t ebp[2] = {0u, 0u};
+        const char* xp[P::BPL];
+        int valid[P::BPL];
+        int eb[P::BPL];
+        bool pois[P::BPL];
         int local = kNoBlock;
+        // pass 1: block exponents
 #pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-            uint32_t m;
+        for (int i = 0; i < P::BPL; ++i) {
+            const int q = i * P::NT + t;  // block of the tile: row q/4, column block q%4
+            const int64_t row = ti * 128 + (q >> 2), col0 = tj * 128 + (q & 3) * 32;
+            valid[i] = row < a.rows ? (int)max((int64_t)0, min((int64_t)32, a.K - col0)) : 0;
+            xp[i] = static_cast<const char*>(a.x) + (row * a.ldx + col0) * P::ES;
+            uint32_t v[P::SEGS][8];
+            load_blk<ELT, VEC, 1>(v, xp[i], valid[i]);
+            uint32_t m = 0u;
             if constexpr (ELT == Elt::BF16) {
-                const uint32_t M = 0x7FFF7FFFu;
-                m = u16x2_max(u16x2_max(v[i].x & M, v[i].y & M), u16x2_max(v[i].z & M, v[i].w & M));
-                m = u16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                m = u16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+#pragma unroll
+                for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) m = u16x2_max(m, v[s][k] & 0x7FFF7FFFu);
                 m = max(m & 0xFFFFu, m >> 16);
-                if (m >= 0x7F80u) m = 0xFFFFFFFFu;
+                pois[i] = m >= 0x7F80u;
             } else {
-                const uint32_t M = 0x7FFFFFFFu;
-                m = max(max(v[i].x & M, v[i].y & M), max(v[i].z & M, v[i].w & M));
-                m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                if (m >= 0x7F800000u) m = 0xFFFFFFFFu;
+#pragma unroll
+                for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) m = max(m, v[s][k] & 0x7FFFFFFFu);
+                pois[i] = m >= 0x7F800000u;
             }
-            const int e = block_exponent<P::MANT>(m);
-            const uint32_t byte = m == 0xFFFFFFFFu ? 0xFFu : (uint32_t)(e + 126);  // 0..251
-            ebp[i >> 2] |= byte << ((i & 3) * 8);
-            if (m != 0xFFFFFFFFu) local = max(local, e);
+            eb[i] = block_exponent<P::MANT>(m);
+            if (!pois[i] && valid[i] > 0) local = max(local, eb[i]);
         }
         local = __reduce_max_sync(0xffffffffu, local);
         if ((t & 31) == 0) warp_max[t >> 5] = local;
@@ -108,58 +122,77 @@ __global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB) block128_kerne
         const int T = max(emax - 6, -127);
         if (t == 0) reinterpret_cast<uint32_t*>(a.tile_scale_inv)[ti * tiles_c + tj] = f32_pow2(T);
 
-        uint8_t* dp = a.data + row0 * a.K + col0;
+        // pass 2: encode
 #pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-            const uint32_t byte = (ebp[i >> 2] >> ((i & 3) * 8)) & 0xFFu;
-            const bool poisoned = byte == 0xFFu;
-            const int eb = (int)byte - 126;
-            const uint32_t fold = f32_pow2(max(eb - T, -126));
-            uint32_t lo, hi;
+        for (int i = 0; i < P::BPL; ++i) {
+            if (valid[i] <= 0) continue;
+            uint32_t v[P::SEGS][8];
+            load_blk<ELT, VEC, 2>(v, xp[i], valid[i]);
+            // RTNE onto E4M3 of p * 2^(e_b - T): the grid value p is exact in
+            // bf16/fp32, the power-of-two fold is exact in fp32 (or far below
+            // E4M3's smallest subnormal), and cvt rounds once.
+            const uint32_t fold = f32_pow2(max(eb[i] - T, -126));
+            uint32_t b[8];
             if constexpr (ELT == Elt::BF16) {
-                const Bf16Grid g = bf16_grid_unit(eb);
-                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-                uint32_t b[4];
+                const Bf16Grid g = bf16_grid_unit(eb[i]);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t s = bf2_grid(w[k] & 0x7FFF7FFFu, g) | (w[k] & 0x80008000u);
-                    b[k] = e4m3x2_from_f32(f32_mul(s & 0xFFFF0000u, fold), f32_mul(s << 16, fold));
-                }
-                lo = b[0] | (b[1] << 16);
-                hi = b[2] | (b[3] << 16);
+                for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t h[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const uint32_t w = v[s][2 * q + u];
+                            const uint32_t sg = bf2_grid(w & 0x7FFF7FFFu, g) | (w & 0x80008000u);
+                            h[u] = e4m3x2_from_f32(f32_mul(sg & 0xFFFF0000u, fold), f32_mul(sg << 16, fold));
+                        }
+                        b[4 * s + q] = h[0] | (h[1] << 16);
+                    }
             } else {
-                const uint32_t mult = f32_pow2(-eb);
-                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-                uint32_t u[4];
+                const uint32_t mult = f32_pow2(-eb[i]);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    u[k] = f32_mul(f32_grid(w[k] & 0x7FFFFFFFu, mult) | (w[k] & 0x80000000u), fold);
-                lo = e4m3x2_from_f32(u[1], u[0]) | (e4m3x2_from_f32(u[3], u[2]) << 16);
-                hi = 0u;
+                for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t u4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t w = v[s][4 * q + u];
+                            u4[u] = f32_mul(f32_grid(w & 0x7FFFFFFFu, mult) | (w & 0x80000000u), fold);
+                        }
+                        b[2 * s + q] = e4m3x2_from_f32(u4[1], u4[0]) | (e4m3x2_from_f32(u4[3], u4[2]) << 16);
+                    }
             }
-            if (poisoned) lo = hi = 0x7F7F7F7Fu;
-            if (16 * i >= nvalid) continue;
-            uint8_t* d = dp + (int64_t)i * 16 * a.K;
-            if constexpr (VEC) {
-                if constexpr (ELT == Elt::BF16)
-                    __stcs(reinterpret_cast<uint2*>(d), make_uint2(lo, hi));
-                else
-                    __stcs(reinterpret_cast<unsigned int*>(d), lo);
+            if (pois[i])
+#pragma unroll
+                for (int k = 0; k < 8; ++k) b[k] = 0x7F7F7F7Fu;
+            const int q = i * P::NT + t;
+            uint8_t* d = a.data + (ti * 128 + (q >> 2)) * a.K + tj * 128 + (q & 3) * 32;
+            if constexpr (DST == 2) {
+                st32(d, b);
+            } else if constexpr (DST == 1) {
+                st16(d, b[0], b[1], b[2], b[3]);
+                if (valid[i] > 16) st16(d + 16, b[4], b[5], b[6], b[7]);
             } else {
 #pragma unroll
-                for (int k = 0; k < P::CH; ++k)
-                    if (col0 + k < a.K) d[k] = (uint8_t)((k < 4 ? lo : hi) >> ((k & 3) * 8));
+                for (int k = 0; k < 32; ++k)
+                    if (k < valid[i]) d[k] = (uint8_t)(b[k >> 2] >> ((k & 3) * 8));
             }
         }
     }
 }
 
-template <Elt ELT, bool VEC>
+template <Elt ELT, bool VEC, int DST>
 cudaError_t launch_one(const Block128Args& a, cudaStream_t s) {
     const int64_t tr = ceil_div(a.rows, 128), tc = ceil_div(a.K, 128);
     if (tc > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const unsigned gy = (unsigned)(tr < 65535 ? tr : 65535);
-    block128_kernel<ELT, VEC><<<dim3((unsigned)tc, gy), T128<ELT>::NT, 0, s>>>(a, tr, tc);
+    static bool configured = false;
+    if (!configured) {  // no shared memory to speak of: give L1 the whole carveout
+        cudaFuncSetAttribute(block128_kernel<ELT, VEC, DST>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
+        configured = true;
+    }
+    block128_kernel<ELT, VEC, DST><<<dim3((unsigned)tc, gy), T128<ELT>::NT, 0, s>>>(a, tr, tc);
     return cudaGetLastError();
 }
 
@@ -168,9 +201,12 @@ bool aligned(const void* p, int64_t n) { return (reinterpret_cast<uintptr_t>(p) 
 template <Elt ELT>
 cudaError_t dispatch(const Block128Args& a, cudaStream_t s) {
     using P = T128<ELT>;
-    const bool vec =
-        aligned(a.x, 16) && (a.ldx * P::ES) % 16 == 0 && a.K % P::CH == 0 && aligned(a.data, P::CH);
-    return vec ? launch_one<ELT, true>(a, s) : launch_one<ELT, false>(a, s);
+    const bool vec = aligned(a.x, 32) && (a.ldx * P::ES) % 32 == 0 && (a.K * P::ES) % 32 == 0;
+    const int dst = (aligned(a.data, 32) && a.K % 32 == 0) ? 2 : (aligned(a.data, 16) && a.K % 16 == 0) ? 1 : 0;
+    if (!vec) return launch_one<ELT, false, 0>(a, s);
+    if (dst == 2) return launch_one<ELT, true, 2>(a, s);
+    if (dst == 1) return launch_one<ELT, true, 1>(a, s);
+    return launch_one<ELT, true, 0>(a, s);
 }
 
 }  // namespace

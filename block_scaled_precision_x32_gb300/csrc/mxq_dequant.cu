@@ -5,10 +5,21 @@
 // weight QAT on MXFP8 and FP8 block-scaling recipes", Description (UE8M0
 // code 0 decodes to 2^-127, code 255 to NaN).
 //
-// Each thread takes 16 payload bytes (one half of a 1x32 block, inside one
-// 128x128 tile), decodes them by placing the fp8 fields in an fp32 pattern
-// and multiplying by 2^120 (E4M3) or 2^112 (E5M2) -- exact, subnormals
-// included -- then multiplies by the scale with IEEE fp32 rounding.
+// Each lane owns whole 1x32 blocks: 32 payload bytes (one 32-byte load),
+// one scale, 64 (bf16) or 128 (fp32) output bytes in 32-byte stores.
+//
+// MXFP8 fast path.  Placing the E4M3 (E5M2) fields of a payload byte at
+// bits 10..4 (11..3) of a bf16 pattern gives payload * 2^-120 (2^-112)
+// exactly, subnormals included; one exact bf16 multiply by 2^120 (2^112)
+// and one by the scale 2^(code-127) -- a single round-to-nearest-even of
+// the exact product -- give the bf16 result.  That equals rounding the
+// exact fp32 product to bf16, because the fp32 product of a <= 4-bit
+// significand and a power of two is exact.  For fp32 output the bf16 value
+// is exact whenever the product stays normal (code >= 10 for E4M3, >= 17 for
+// E5M2).  Blocks with a NaN or Inf payload, scale code 255, or a smaller
+// code for fp32 output take the element-wise fp32 path, which also makes
+// NaN canonical.  The 128x128 form multiplies by an arbitrary fp32
+// scale_inv and always takes the fp32 path.
 #include <cuda_runtime.h>
 
 #include "mxq_device.cuh"
@@ -18,7 +29,6 @@ namespace mxq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kItems = 2;
 
 __device__ __forceinline__ int64_t scale_offset(int64_t r, int64_t j, int64_t nb, int64_t Cp, int lay) {
     if (lay == 0) return r * nb + j;
@@ -26,13 +36,13 @@ __device__ __forceinline__ int64_t scale_offset(int64_t r, int64_t j, int64_t nb
     return ((r >> 7) * (Cp >> 2) + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
 }
 
-// fp8 byte -> exact fp32 pattern times `scale`, NaN made canonical.
+// fp8 byte -> exact fp32 pattern times `scale` (IEEE fp32 product), NaN made canonical.
 template <bool E5M2>
 __device__ __forceinline__ uint32_t decode_scaled(uint32_t b, uint32_t scale) {
     const uint32_t mag = b & 0x7Fu;
     uint32_t f;
     bool nan;
-    if (E5M2) {
+    if constexpr (E5M2) {
         f = f32_mul((mag << 21) | ((b & 0x80u) << 24), 0x77800000u);  // * 2^112
         nan = mag > 0x7Cu;
         if (mag == 0x7Cu) f = 0x7F800000u | ((b & 0x80u) << 24);
@@ -48,131 +58,199 @@ __device__ __forceinline__ uint32_t decode_scaled(uint32_t b, uint32_t scale) {
 // canonical, overflow goes to Inf).
 __device__ __forceinline__ uint32_t bf16_rne(uint32_t u) { return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16; }
 
-template <bool E5M2, bool BF16OUT, bool VEC>
-__global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a, int64_t cpr, int64_t step_r,
-                                                           int64_t step_c) {
-    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const int64_t S = (int64_t)gridDim.x * kThreads;
-    const int64_t total = a.rows * cpr;
-    const int64_t nb = (a.K + 31) >> 5;
-    const int64_t Cp = (nb + 3) & ~int64_t(3);
-    const int64_t tc = (a.K + 127) >> 7;
+// Any byte of w a NaN/Inf payload?  (E4M3: low 7 bits all ones; E5M2:
+// exponent all ones.)
+template <bool E5M2>
+__device__ __forceinline__ uint32_t special_bytes(uint32_t w) {
+    if constexpr (E5M2)
+        return ((w & 0x7C7C7C7Cu) + 0x04040404u) & 0x80808080u;
+    else
+        return ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+}
 
-    int64_t r[kItems], cc[kItems];
+// Payload bytes (lo, hi) of one word's pair -> bf16x2 of payload * 2^-120 / 2^-112.
+template <bool E5M2>
+__device__ __forceinline__ uint32_t place_pair(uint32_t w, uint32_t sel) {
+    const uint32_t t = prmt(w, 0u, sel);  // byte k of the pair at bits 16k..16k+7
+    constexpr int SH = E5M2 ? 5 : 4;
+    return ((t & 0x007F007Fu) << SH) | ((t & 0x00800080u) << 8);
+}
+
+template <int SRC>
+__device__ __forceinline__ void load_payload(uint32_t (&w)[8], const uint8_t* p, int valid) {
+    if constexpr (SRC == 2) {
+        ld32(w, p);
+    } else if constexpr (SRC == 1) {
+        const uint4 a = *reinterpret_cast<const uint4*>(p);
+        w[0] = a.x;
+        w[1] = a.y;
+        w[2] = a.z;
+        w[3] = a.w;
+        if (valid > 16) {
+            const uint4 b = *reinterpret_cast<const uint4*>(p + 16);
+            w[4] = b.x;
+            w[5] = b.y;
+            w[6] = b.z;
+            w[7] = b.w;
+        } else {
+            w[4] = w[5] = w[6] = w[7] = 0u;
+        }
+    } else {
 #pragma unroll
-    for (int u = 0; u < kItems; ++u) {
-        const int64_t w = tid + u * S;
-        r[u] = w / cpr;
-        cc[u] = w - r[u] * cpr;
+        for (int k = 0; k < 8; ++k) w[k] = 0u;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < valid) w[i >> 2] |= (uint32_t)p[i] << ((i & 3) * 8);
     }
-    for (int64_t wb = tid; wb < total; wb += kItems * S) {
-        uint4 v[kItems];
-        uint32_t scale[kItems];
+}
+
+// out: 32 results as bf16 (16 words) or fp32 (32 words); VOUT: 32-byte stores.
+template <bool BF16OUT, bool VOUT>
+__device__ __forceinline__ void store_out(void* out, const uint32_t* o, int valid) {
+    constexpr int WORDS = BF16OUT ? 16 : 32;
+    constexpr int EPS = BF16OUT ? 16 : 8;  // elements per 32-byte segment
+    if constexpr (VOUT) {
 #pragma unroll
-        for (int u = 0; u < kItems; ++u) {
-            const int64_t col0 = cc[u] * 16;
-            const bool ok = r[u] < a.rows;
-            v[u] = make_uint4(0u, 0u, 0u, 0u);
-            scale[u] = 0u;
-            if (!ok) continue;
-            const uint8_t* drow = a.data + r[u] * a.K;
-            if (VEC) {
-                v[u] = __ldcs(reinterpret_cast<const uint4*>(drow + col0));
-            } else {
-                uint32_t w[4] = {0u, 0u, 0u, 0u};
+        for (int s = 0; s < WORDS / 8; ++s) {
+            if (s * EPS < valid) {
+                uint32_t seg[8];
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    if (col0 + k < a.K) w[k >> 2] |= (uint32_t)drow[col0 + k] << ((k & 3) * 8);
-                v[u] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            if (a.kind == 0) {
-                const uint32_t c = a.scales[scale_offset(r[u], col0 >> 5, nb, Cp, a.lay)];
-                scale[u] = c == 255u ? 0x7FC00000u : f32_pow2((int)c - 127);
-            } else {
-                scale[u] = reinterpret_cast<const uint32_t*>(a.tile_scale_inv)[(r[u] >> 7) * tc + (col0 >> 7)];
+                for (int k = 0; k < 8; ++k) seg[k] = o[8 * s + k];
+                st32(static_cast<char*>(out) + 32 * s, seg);
             }
         }
+    } else {
 #pragma unroll
-        for (int u = 0; u < kItems; ++u) {
-            if (r[u] >= a.rows) continue;
-            const int64_t col0 = cc[u] * 16;
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            uint32_t o[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) o[k] = decode_scaled<E5M2>((w[k >> 2] >> ((k & 3) * 8)) & 0xFFu, scale[u]);
-            if (BF16OUT) {
-                uint32_t h[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) h[k] = bf16_rne(o[2 * k]) | (bf16_rne(o[2 * k + 1]) << 16);
-                uint16_t* orow = static_cast<uint16_t*>(a.out) + r[u] * a.K;
-                if (VEC) {
-                    __stcs(reinterpret_cast<uint4*>(orow + col0), make_uint4(h[0], h[1], h[2], h[3]));
-                    __stcs(reinterpret_cast<uint4*>(orow + col0 + 8), make_uint4(h[4], h[5], h[6], h[7]));
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        if (col0 + k < a.K) orow[col0 + k] = (uint16_t)(h[k >> 1] >> ((k & 1) * 16));
-                }
-            } else {
-                uint32_t* orow = static_cast<uint32_t*>(a.out) + r[u] * a.K;
-                if (VEC) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        __stcs(reinterpret_cast<uint4*>(orow + col0 + 4 * q),
-                               make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        if (col0 + k < a.K) orow[col0 + k] = o[k];
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kItems; ++u) {
-            cc[u] += step_c;
-            r[u] += step_r;
-            if (cc[u] >= cpr) {
-                cc[u] -= cpr;
-                r[u] += 1;
+        for (int i = 0; i < 32; ++i) {
+            if (i < valid) {
+                if constexpr (BF16OUT)
+                    static_cast<uint16_t*>(out)[i] = (uint16_t)(o[i >> 1] >> ((i & 1) * 16));
+                else
+                    static_cast<uint32_t*>(out)[i] = o[i];
             }
         }
     }
 }
 
-template <bool E5M2, bool BF16OUT, bool VEC>
+template <int KIND, bool E5M2, bool BF16OUT, int SRC, bool VOUT>
+__global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a, int64_t nb, int64_t step_r,
+                                                           int64_t step_c) {
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t S = (int64_t)gridDim.x * kThreads;
+    const int64_t total = a.rows * nb;
+    const int64_t Cp = (nb + 3) & ~int64_t(3);
+    const int64_t tc = (a.K + 127) >> 7;
+    int64_t r = tid / nb, j = tid - (tid / nb) * nb;
+    constexpr int WORDS = BF16OUT ? 16 : 32;
+
+    for (int64_t wi = tid; wi < total; wi += S) {
+        const int64_t col0 = j * 32;
+        const int valid = (int)min((int64_t)32, a.K - col0);
+        uint32_t w[8];
+        load_payload<SRC>(w, a.data + r * a.K + col0, valid);
+        uint32_t scale32;  // fp32 multiplier of the element-wise path
+        bool fast = false;
+        uint32_t scale16 = 0u;  // bf16x2 2^(code-127) of the fast path
+        if constexpr (KIND == 0) {
+            const uint32_t c = a.scales[scale_offset(r, j, nb, Cp, a.lay)];
+            scale32 = c == 255u ? 0x7FC00000u : f32_pow2((int)c - 127);
+            uint32_t sp = 0u;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sp |= special_bytes<E5M2>(w[k]);
+            fast = sp == 0u && c != 255u && (BF16OUT || c >= (E5M2 ? 17u : 10u));
+            scale16 = c == 0u ? 0x00400040u : ((c << 7) | (c << 23));
+        } else {
+            scale32 = reinterpret_cast<const uint32_t*>(a.tile_scale_inv)[(r >> 7) * tc + (col0 >> 7)];
+        }
+        uint32_t o[WORDS];
+        if (KIND == 0 && fast) {
+            const uint32_t fix = E5M2 ? 0x77807780u : 0x7B807B80u;  // 2^112 / 2^120, both halves
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t pr = place_pair<E5M2>(w[k], h ? 0x4342u : 0x4140u);
+                    const uint32_t y = bf2_mul(bf2_mul(pr, fix), scale16);
+                    if constexpr (BF16OUT) {
+                        o[2 * k + h] = y;
+                    } else {
+                        o[4 * k + 2 * h] = y << 16;
+                        o[4 * k + 2 * h + 1] = y & 0xFFFF0000u;
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const uint32_t f = decode_scaled<E5M2>((w[i >> 2] >> ((i & 3) * 8)) & 0xFFu, scale32);
+                if constexpr (BF16OUT) {
+                    if (i & 1)
+                        o[i >> 1] |= bf16_rne(f) << 16;
+                    else
+                        o[i >> 1] = bf16_rne(f);
+                } else {
+                    o[i] = f;
+                }
+            }
+        }
+        char* op = static_cast<char*>(a.out) + (r * a.K + col0) * (BF16OUT ? 2 : 4);
+        store_out<BF16OUT, VOUT>(op, o, valid);
+
+        j += step_c;
+        r += step_r;
+        if (j >= nb) {
+            j -= nb;
+            r += 1;
+        }
+    }
+}
+
+template <int KIND, bool E5M2, bool BF16OUT, int SRC, bool VOUT>
 cudaError_t launch_one(const DequantArgs& a, cudaStream_t s) {
-    const int64_t cpr = ceil_div(a.K, 16);
-    const int64_t total = a.rows * cpr;
+    const int64_t nb = ceil_div(a.K, 32);
+    const int64_t total = a.rows * nb;
     static int occ = 0;
     if (occ == 0) {
-        cudaError_t err =
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dequant_kernel<E5M2, BF16OUT, VEC>, kThreads, 0);
+        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &occ, dequant_kernel<KIND, E5M2, BF16OUT, SRC, VOUT>, kThreads, 0);
         if (err != cudaSuccess) return err;
         if (occ < 1) occ = 1;
     }
-    int64_t grid = ceil_div(total, (int64_t)kThreads * kItems);
+    int64_t grid = ceil_div(total, (int64_t)kThreads);
     const int64_t resident = (int64_t)sm_count() * occ;
     if (grid > resident) grid = resident;
     if (grid < 1) grid = 1;
-    const int64_t stride = grid * kThreads * kItems;
-    dequant_kernel<E5M2, BF16OUT, VEC><<<(unsigned)grid, kThreads, 0, s>>>(a, cpr, stride / cpr, stride % cpr);
+    const int64_t stride = grid * kThreads;
+    dequant_kernel<KIND, E5M2, BF16OUT, SRC, VOUT><<<(unsigned)grid, kThreads, 0, s>>>(a, nb, stride / nb,
+                                                                                       stride % nb);
     return cudaGetLastError();
 }
 
 bool aligned(const void* p, int64_t n) { return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)n) == 0; }
 
-template <bool E5M2, bool BF16OUT>
-cudaError_t pick_vec(const DequantArgs& a, cudaStream_t s) {
-    const bool vec = aligned(a.data, 16) && aligned(a.out, 16) && a.K % 16 == 0;
-    return vec ? launch_one<E5M2, BF16OUT, true>(a, s) : launch_one<E5M2, BF16OUT, false>(a, s);
+template <int KIND, bool E5M2, bool BF16OUT>
+cudaError_t pick_paths(const DequantArgs& a, cudaStream_t s) {
+    const int src = (aligned(a.data, 32) && a.K % 32 == 0) ? 2 : (aligned(a.data, 16) && a.K % 16 == 0) ? 1 : 0;
+    const int es = BF16OUT ? 2 : 4;
+    const bool vout = aligned(a.out, 32) && (a.K * es) % 32 == 0;
+    if (src == 2) return vout ? launch_one<KIND, E5M2, BF16OUT, 2, true>(a, s) : launch_one<KIND, E5M2, BF16OUT, 2, false>(a, s);
+    if (src == 1) return vout ? launch_one<KIND, E5M2, BF16OUT, 1, true>(a, s) : launch_one<KIND, E5M2, BF16OUT, 1, false>(a, s);
+    return launch_one<KIND, E5M2, BF16OUT, 0, false>(a, s);
+}
+
+template <int KIND>
+cudaError_t pick_formats(const DequantArgs& a, cudaStream_t s) {
+    const bool e5 = a.fp8 == 1;
+    if (e5) return a.out_bf16 ? pick_paths<KIND, true, true>(a, s) : pick_paths<KIND, true, false>(a, s);
+    return a.out_bf16 ? pick_paths<KIND, false, true>(a, s) : pick_paths<KIND, false, false>(a, s);
 }
 
 }  // namespace
 
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s) {
-    const bool e5 = a.fp8 == 1;
-    if (e5) return a.out_bf16 ? pick_vec<true, true>(a, s) : pick_vec<true, false>(a, s);
-    return a.out_bf16 ? pick_vec<false, true>(a, s) : pick_vec<false, false>(a, s);
+    if (a.kind == 0) return pick_formats<0>(a, s);
+    // the 128x128 form carries E4M3 payloads only (checked by the caller)
+    return a.out_bf16 ? pick_paths<1, false, true>(a, s) : pick_paths<1, false, false>(a, s);
 }
 
 }  // namespace mxq

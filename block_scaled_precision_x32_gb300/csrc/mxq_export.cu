@@ -7,8 +7,10 @@
 //
 // Swizzled input: one CTA per (128-row tile, group of 32 column tiles).
 // The group's bytes are contiguous in the swizzled buffer (32 x 512), so
-// they are staged in shared memory with 16-byte loads and written out row
-// by row, consecutive threads on consecutive output bytes.
+// they are staged in shared memory with 16-byte loads -- each 512-byte tile
+// padded by one word so that lanes reading the same word of consecutive
+// tiles hit distinct banks -- and written out row by row, consecutive lanes
+// on consecutive output words (4 scales) or bytes.
 // Padded input: one warp per row, lanes on consecutive bytes.
 #include <cuda_runtime.h>
 
@@ -18,32 +20,52 @@ namespace mxq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kGroup = 32;  // column tiles (4 scale columns each) per CTA
+constexpr int kGroup = 32;        // column tiles (4 scale columns each) per CTA
+constexpr int kTileWords = 129;   // 128 words of a 512-byte tile + 1 pad word
 
-template <bool VEC>
+template <bool VEC_IN, bool WORD_OUT>
 __global__ void __launch_bounds__(kThreads) unswizzle_kernel(ExportArgs a, int64_t tiles_r) {
-    __shared__ __align__(16) uint8_t tile[kGroup * 512];
+    __shared__ uint32_t tile[kGroup * kTileWords];
     const int64_t nb = (a.K + 31) >> 5;
     const int64_t Cp = (nb + 3) & ~int64_t(3);
     const int64_t ct = Cp >> 2;  // column tiles per row tile
     const int64_t jt0 = (int64_t)blockIdx.x * kGroup;
-    const int64_t g = min((int64_t)kGroup, ct - jt0);
-    const int64_t W = min(4 * g, nb - 4 * jt0);  // output columns of this group
+    const int g = (int)min((int64_t)kGroup, ct - jt0);
+    const int W = (int)min((int64_t)4 * g, nb - 4 * jt0);  // output columns of this group
     for (int64_t rt = blockIdx.y; rt < tiles_r; rt += gridDim.y) {
         const uint8_t* src = a.scales + (rt * ct + jt0) * 512;
-        if (VEC) {
-            for (int64_t i = threadIdx.x; i < g * 32; i += kThreads)
-                reinterpret_cast<uint4*>(tile)[i] = reinterpret_cast<const uint4*>(src)[i];
+        if constexpr (VEC_IN) {
+            for (int i = threadIdx.x; i < g * 32; i += kThreads) {
+                const uint4 q = reinterpret_cast<const uint4*>(src)[i];
+                uint32_t* d = tile + (i >> 5) * kTileWords + (i & 31) * 4;
+                d[0] = q.x;
+                d[1] = q.y;
+                d[2] = q.z;
+                d[3] = q.w;
+            }
         } else {
-            for (int64_t i = threadIdx.x; i < g * 512; i += kThreads) tile[i] = src[i];
+            for (int i = threadIdx.x; i < g * 128; i += kThreads) {
+                const uint8_t* b = src + 4 * i;
+                tile[(i >> 7) * kTileWords + (i & 127)] =
+                    b[0] | ((uint32_t)b[1] << 8) | ((uint32_t)b[2] << 16) | ((uint32_t)b[3] << 24);
+            }
         }
         __syncthreads();
         const int64_t r0 = rt * 128;
-        const int64_t nrows = min((int64_t)128, a.rows - r0);
-        for (int64_t idx = threadIdx.x; idx < nrows * W; idx += kThreads) {
-            const int64_t rr = idx / W, j = idx - rr * W;
-            const int64_t off = (j >> 2) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (j & 3);
-            a.out[(r0 + rr) * nb + 4 * jt0 + j] = tile[off];
+        const int nrows = (int)min((int64_t)128, a.rows - r0);
+        if constexpr (WORD_OUT) {
+            // nb % 4 == 0: the 4 scales of a (row, column tile) are one aligned word
+            uint32_t* out = reinterpret_cast<uint32_t*>(a.out);
+            for (int idx = threadIdx.x; idx < nrows * g; idx += kThreads) {
+                const int rr = idx / g, jt = idx - rr * g;
+                out[(r0 + rr) * (nb >> 2) + jt0 + jt] = tile[jt * kTileWords + (rr & 31) * 4 + (rr >> 5)];
+            }
+        } else {
+            for (int idx = threadIdx.x; idx < nrows * W; idx += kThreads) {
+                const int rr = idx / W, j = idx - rr * W;
+                const uint32_t word = tile[(j >> 2) * kTileWords + (rr & 31) * 4 + (rr >> 5)];
+                a.out[(r0 + rr) * nb + 4 * jt0 + j] = (uint8_t)(word >> ((j & 3) * 8));
+            }
         }
         __syncthreads();
     }
@@ -68,11 +90,17 @@ cudaError_t launch_export(const ExportArgs& a, cudaStream_t s) {
         const int64_t tr = ceil_div(a.rows, 128);
         const int64_t gx = ceil_div(ct, kGroup);
         const unsigned gy = (unsigned)(tr < 65535 ? tr : 65535);
-        const bool vec = (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0;
-        if (vec)
-            unswizzle_kernel<true><<<dim3((unsigned)gx, gy), kThreads, 0, s>>>(a, tr);
+        const dim3 grid((unsigned)gx, gy);
+        const bool vin = (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0;
+        const bool wout = nb % 4 == 0 && (reinterpret_cast<uintptr_t>(a.out) & 3) == 0;
+        if (vin && wout)
+            unswizzle_kernel<true, true><<<grid, kThreads, 0, s>>>(a, tr);
+        else if (vin)
+            unswizzle_kernel<true, false><<<grid, kThreads, 0, s>>>(a, tr);
+        else if (wout)
+            unswizzle_kernel<false, true><<<grid, kThreads, 0, s>>>(a, tr);
         else
-            unswizzle_kernel<false><<<dim3((unsigned)gx, gy), kThreads, 0, s>>>(a, tr);
+            unswizzle_kernel<false, false><<<grid, kThreads, 0, s>>>(a, tr);
     } else {
         int64_t grid = ceil_div(a.rows, kThreads / 32);
         const int64_t cap = (int64_t)sm_count() * 8;

@@ -4,13 +4,14 @@
 // TE PR #3264 "MXFP4 weight QAT on MXFP8 and FP8 block-scaling recipes",
 // Description, mode 1 (projection) and mode 2 (direct, MXFP8 rowwise).
 //
-// Work split.  A "chunk" is 16 bytes of one row (8 bf16 or 4 fp32); a 1x32
-// block is L = 4 (bf16) or 8 (fp32) consecutive lanes, so the block amax is
-// two or three xor-shuffles.  Rows are cut into nb*L chunks (chunks past K
-// in a short last block load zeros and store nothing).  Threads walk the
-// flattened (row, chunk) space with a grid stride, kItems chunks in flight
-// per thread, the row/column cursor advanced incrementally.  The grid is a
-// resident multiple of the SM count.
+// Work split.  Each lane owns whole 1x32 blocks: it reads a block as two
+// (bf16) or four (fp32) 32-byte vectors -- one full sector each, so a warp's
+// request is sector-exact -- finds the amax, the scale exponent and the
+// block constants once, converts the 32 elements and writes them back with
+// 32-byte stores.  No shuffles, no shared memory.  Lanes walk the flattened
+// (row, block) space with a grid stride over a resident grid (a multiple of
+// the SM count); the row/block cursor advances by one add per step.
+// Misaligned or ragged views use the same code with element-wise loads.
 #include <cuda_runtime.h>
 
 #include "mxq_device.cuh"
@@ -20,7 +21,6 @@ namespace mxq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kItems = 4;
 
 __device__ __forceinline__ int64_t scale_offset(int64_t r, int64_t j, int64_t nb, int64_t Cp, int lay) {
     if (lay == 0) return r * nb + j;
@@ -32,206 +32,204 @@ template <Elt ELT>
 struct Traits;
 template <>
 struct Traits<Elt::BF16> {
-    static constexpr int ES = 2, CH = 8, L = 4, MANT = 7;
+    static constexpr int ES = 2, SEGS = 2, SEG_ELEMS = 16, MANT = 7;
 };
 template <>
 struct Traits<Elt::FP32> {
-    static constexpr int ES = 4, CH = 4, L = 8, MANT = 23;
+    static constexpr int ES = 4, SEGS = 4, SEG_ELEMS = 8, MANT = 23;
 };
 
+// Load one block (valid = elements present, 1..32) as SEGS x 8 words;
+// missing elements read as +0.
 template <Elt ELT, bool VEC>
-__device__ __forceinline__ uint4 load_chunk(const char* row, int64_t col0, int64_t K, bool ok) {
+__device__ __forceinline__ void load_block(uint32_t (&v)[Traits<ELT>::SEGS][8], const char* p, int valid) {
     using T = Traits<ELT>;
-    if (!ok) return make_uint4(0u, 0u, 0u, 0u);
-    if constexpr (VEC) {
-        return __ldcs(reinterpret_cast<const uint4*>(row + col0 * T::ES));
-    } else {
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int i = 0; i < T::CH; ++i) {
-            const int64_t c = col0 + i;
-            if (c < K) {
-                if constexpr (ELT == Elt::BF16)
-                    w[i >> 1] |= (uint32_t)reinterpret_cast<const uint16_t*>(row)[c] << ((i & 1) * 16);
-                else
-                    w[i] = reinterpret_cast<const uint32_t*>(row)[c];
+    for (int s = 0; s < T::SEGS; ++s) {
+        if constexpr (VEC) {
+            if (s * T::SEG_ELEMS < valid) {
+                ld32(v[s], p + 32 * s);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[s][k] = 0u;
             }
-        }
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
-
-template <Elt ELT, bool VEC>
-__device__ __forceinline__ void store_chunk(char* row, int64_t col0, int64_t K, uint4 v) {
-    using T = Traits<ELT>;
-    if constexpr (VEC) {
-        __stcs(reinterpret_cast<uint4*>(row + col0 * T::ES), v);
-    } else {
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        } else {
 #pragma unroll
-        for (int i = 0; i < T::CH; ++i) {
-            const int64_t c = col0 + i;
-            if (c < K) {
-                if constexpr (ELT == Elt::BF16)
-                    reinterpret_cast<uint16_t*>(row)[c] = (uint16_t)(w[i >> 1] >> ((i & 1) * 16));
-                else
-                    reinterpret_cast<uint32_t*>(row)[c] = w[i];
+            for (int k = 0; k < 8; ++k) {
+                uint32_t w = 0u;
+                if constexpr (ELT == Elt::BF16) {
+                    const int i0 = s * 16 + 2 * k;
+                    if (i0 < valid) w = reinterpret_cast<const uint16_t*>(p)[i0];
+                    if (i0 + 1 < valid) w |= (uint32_t)reinterpret_cast<const uint16_t*>(p)[i0 + 1] << 16;
+                } else {
+                    const int i0 = s * 8 + k;
+                    if (i0 < valid) w = reinterpret_cast<const uint32_t*>(p)[i0];
+                }
+                v[s][k] = w;
             }
         }
     }
 }
 
-// Largest magnitude pattern of the chunk, reduced over the block's lanes.
+template <Elt ELT, bool VEC>
+__device__ __forceinline__ void store_block(char* p, const uint32_t (&y)[Traits<ELT>::SEGS][8], int valid) {
+    using T = Traits<ELT>;
+#pragma unroll
+    for (int s = 0; s < T::SEGS; ++s) {
+        if constexpr (VEC) {
+            if (s * T::SEG_ELEMS < valid) st32(p + 32 * s, y[s]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if constexpr (ELT == Elt::BF16) {
+                    const int i0 = s * 16 + 2 * k;
+                    if (i0 < valid) reinterpret_cast<uint16_t*>(p)[i0] = (uint16_t)y[s][k];
+                    if (i0 + 1 < valid) reinterpret_cast<uint16_t*>(p)[i0 + 1] = (uint16_t)(y[s][k] >> 16);
+                } else {
+                    const int i0 = s * 8 + k;
+                    if (i0 < valid) reinterpret_cast<uint32_t*>(p)[i0] = y[s][k];
+                }
+            }
+        }
+    }
+}
+
+// 32 payload bytes of one block; DST 2: one 32-byte store, 1: two 16-byte
+// stores, 0: bytes.
+template <int DST>
+__device__ __forceinline__ void store_payload(uint8_t* p, const uint32_t (&b)[8], int valid) {
+    if constexpr (DST == 2) {
+        st32(p, b);
+    } else if constexpr (DST == 1) {
+        st16(p, b[0], b[1], b[2], b[3]);
+        if (valid > 16) st16(p + 16, b[4], b[5], b[6], b[7]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < valid) p[i] = (uint8_t)(b[i >> 2] >> ((i & 3) * 8));
+    }
+}
+
 template <Elt ELT>
-__device__ __forceinline__ uint32_t block_amax(uint4 v) {
+__device__ __forceinline__ uint32_t block_amax(const uint32_t (&v)[Traits<ELT>::SEGS][8]) {
+    using T = Traits<ELT>;
     if constexpr (ELT == Elt::BF16) {
-        const uint32_t M = 0x7FFF7FFFu;
-        uint32_t m = u16x2_max(u16x2_max(v.x & M, v.y & M), u16x2_max(v.z & M, v.w & M));
-        m = u16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = u16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        uint32_t m = 0u;
+#pragma unroll
+        for (int s = 0; s < T::SEGS; ++s)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m = u16x2_max(m, v[s][k] & 0x7FFF7FFFu);
         return max(m & 0xFFFFu, m >> 16);
     } else {
-        const uint32_t M = 0x7FFFFFFFu;
-        uint32_t m = max(max(v.x & M, v.y & M), max(v.z & M, v.w & M));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        uint32_t m = 0u;
+#pragma unroll
+        for (int s = 0; s < T::SEGS; ++s)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m = max(m, v[s][k] & 0x7FFFFFFFu);
         return m;
     }
 }
 
-// Projection of one chunk: sign(x) * p * 2^e.
-template <Elt ELT>
-__device__ __forceinline__ uint4 project_chunk(uint4 v, int e, bool poisoned) {
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    if constexpr (ELT == Elt::BF16) {
-        const Bf16Grid g = bf16_grid_unit(e);
-        const uint32_t scl = bf16_pow2_pair(e);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t t = bf2_grid(w[i] & 0x7FFF7FFFu, g);
-            w[i] = poisoned ? 0x7FC07FC0u : (bf2_mul(t, scl) | (w[i] & 0x80008000u));
-        }
-    } else {
-        const uint32_t mult = f32_pow2(-e), scl = f32_pow2(e);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t t = f32_grid(w[i] & 0x7FFFFFFFu, mult);
-            w[i] = poisoned ? 0x7FC00000u : (f32_mul(t, scl) | (w[i] & 0x80000000u));
-        }
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Fixed-shift-6 lift of one chunk into E4M3 payload bytes (8 for bf16 in a
-// uint2, 4 for fp32 in .x).  code = max(e + 121, 0) is the UE8M0 scale; the
-// payload is p * 2^(e + 127 - code).
-template <Elt ELT>
-__device__ __forceinline__ uint2 mxfp8_chunk(uint4 v, int e, int code, bool poisoned) {
-    const int shift = e + 127 - code;  // 6, or 1..5 when the scale code is clamped at 0
-    if constexpr (ELT == Elt::BF16) {
-        // Round in a domain where the payload P appears as P * 2^(-120 + 16k):
-        // there the bf16 exponent field is the E4M3 one plus 16k, so bits
-        // 10..4 of each bf16 pattern are the E4M3 exponent and mantissa.  k
-        // keeps the multiplier 2^(7 - code + 16k) a normal bf16.
-        const int k = code > 133 ? (code - 133 + 15) >> 4 : 0;
-        Bf16Grid g;
-        g.mult = bf16_pow2_pair(7 - code + 16 * k);
-        g.floor = bf16_pow2_pair(shift - 120 + 16 * k);
-        g.sat = g.floor + 0x01400140u;  // 6 * floor
-        const uint32_t t0 = bf2_grid(v.x & 0x7FFF7FFFu, g);
-        const uint32_t t1 = bf2_grid(v.y & 0x7FFF7FFFu, g);
-        const uint32_t t2 = bf2_grid(v.z & 0x7FFF7FFFu, g);
-        const uint32_t t3 = bf2_grid(v.w & 0x7FFF7FFFu, g);
-        uint32_t lo = lop_select(prmt(t0 >> 4, t1 >> 4, 0x6420u), prmt(v.x, v.y, 0x7531u), 0x7F7F7F7Fu);
-        uint32_t hi = lop_select(prmt(t2 >> 4, t3 >> 4, 0x6420u), prmt(v.z, v.w, 0x7531u), 0x7F7F7F7Fu);
-        if (poisoned) lo = hi = 0x7F7F7F7Fu;
-        return make_uint2(lo, hi);
-    } else {
-        const uint32_t mult = f32_pow2(-e), up = f32_pow2(shift);
-        uint32_t p[4];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            p[i] = f32_mul(f32_grid(w[i] & 0x7FFFFFFFu, mult), up) | (w[i] & 0x80000000u);
-        uint32_t out = e4m3x2_from_f32(p[1], p[0]) | (e4m3x2_from_f32(p[3], p[2]) << 16);
-        if (poisoned) out = 0x7F7F7F7Fu;
-        return make_uint2(out, 0u);
-    }
-}
-
-template <Elt ELT, bool VEC>
-__device__ __forceinline__ void store_payload(uint8_t* drow, int64_t col0, int64_t K, uint2 b) {
-    using T = Traits<ELT>;
-    if constexpr (VEC) {
-        if constexpr (ELT == Elt::BF16)
-            __stcs(reinterpret_cast<uint2*>(drow + col0), b);
-        else
-            __stcs(reinterpret_cast<unsigned int*>(drow + col0), b.x);
-    } else {
-#pragma unroll
-        for (int i = 0; i < T::CH; ++i) {
-            const int64_t c = col0 + i;
-            if (c < K) drow[c] = (uint8_t)((i < 4 ? b.x : b.y) >> ((i & 3) * 8));
-        }
-    }
-}
-
-template <RowMode MODE, Elt ELT, bool VEC>
-__global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_t cpr, int64_t step_r,
+template <RowMode MODE, Elt ELT, bool VEC, int DST>
+__global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_t nb, int64_t step_r,
                                                            int64_t step_c) {
     using T = Traits<ELT>;
-    const int lane = threadIdx.x & 31;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t S = (int64_t)gridDim.x * kThreads;
-    const int64_t total = a.rows * cpr;
-    const int64_t nb = (a.K + 31) >> 5;
+    const int64_t total = a.rows * nb;
     const int64_t Cp = (nb + 3) & ~int64_t(3);
+    int64_t r = tid / nb, j = tid - (tid / nb) * nb;
 
-    int64_t r[kItems], cc[kItems];
-#pragma unroll
-    for (int u = 0; u < kItems; ++u) {
-        const int64_t w = tid + u * S;
-        r[u] = w / cpr;
-        cc[u] = w - r[u] * cpr;
-    }
+    for (int64_t w = tid; w < total; w += S) {
+        const int64_t col0 = j * 32;
+        const int valid = (int)min((int64_t)32, a.K - col0);
+        const char* xp = static_cast<const char*>(a.x) + (r * a.ldx + col0) * T::ES;
+        uint32_t v[T::SEGS][8];
+        load_block<ELT, VEC>(v, xp, valid);
 
-    for (int64_t wbase = tid - lane; wbase < total; wbase += kItems * S) {
-        uint4 v[kItems];
+        const uint32_t amax = block_amax<ELT>(v);
+        const bool poisoned = amax >= (ELT == Elt::BF16 ? 0x7F80u : 0x7F800000u);
+        const int e = block_exponent<T::MANT>(amax);
+
+        if constexpr (MODE == RowMode::PROJECT) {
+            uint32_t y[T::SEGS][8];
+            if constexpr (ELT == Elt::BF16) {
+                const Bf16Grid g = bf16_grid_unit(e);
+                const uint32_t scl = bf16_pow2_pair(e);
 #pragma unroll
-        for (int u = 0; u < kItems; ++u) {
-            const bool ok = r[u] < a.rows && cc[u] * T::CH < a.K;
-            const char* xrow = static_cast<const char*>(a.x) + (ok ? r[u] * a.ldx * T::ES : 0);
-            v[u] = load_chunk<ELT, VEC>(xrow, cc[u] * T::CH, a.K, ok);
-        }
+                for (int s = 0; s < T::SEGS; ++s)
 #pragma unroll
-        for (int u = 0; u < kItems; ++u) {
-            const uint32_t amax = block_amax<ELT>(v[u]);
-            const bool poisoned = amax >= (ELT == Elt::BF16 ? 0x7F80u : 0x7F800000u);
-            const int e = block_exponent<T::MANT>(amax);
-            const bool ok = r[u] < a.rows && cc[u] * T::CH < a.K;
-            const int64_t col0 = cc[u] * T::CH;
-            if constexpr (MODE == RowMode::PROJECT) {
-                const uint4 y = project_chunk<ELT>(v[u], e, poisoned);
-                if (ok) store_chunk<ELT, VEC>(static_cast<char*>(a.y) + r[u] * a.ldy * T::ES, col0, a.K, y);
+                    for (int k = 0; k < 8; ++k)
+                        y[s][k] = bf2_mul(bf2_grid(v[s][k] & 0x7FFF7FFFu, g), scl) | (v[s][k] & 0x80008000u);
+                if (poisoned)
+#pragma unroll
+                    for (int s = 0; s < T::SEGS; ++s)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) y[s][k] = 0x7FC07FC0u;
             } else {
-                const int code = poisoned ? 255 : max(e + 121, 0);
-                const uint2 b = mxfp8_chunk<ELT>(v[u], poisoned ? 0 : e, poisoned ? 0 : code, poisoned);
-                if (ok) {
-                    store_payload<ELT, VEC>(a.data + r[u] * a.K, col0, a.K, b);
-                    if ((lane & (T::L - 1)) == 0)
-                        a.scales[scale_offset(r[u], cc[u] / T::L, nb, Cp, a.lay)] = (uint8_t)code;
-                }
-            }
-        }
+                const uint32_t mult = f32_pow2(-e), scl = f32_pow2(e);
 #pragma unroll
-        for (int u = 0; u < kItems; ++u) {
-            cc[u] += step_c;
-            r[u] += step_r;
-            if (cc[u] >= cpr) {
-                cc[u] -= cpr;
-                r[u] += 1;
+                for (int s = 0; s < T::SEGS; ++s)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        y[s][k] = f32_mul(f32_grid(v[s][k] & 0x7FFFFFFFu, mult), scl) | (v[s][k] & 0x80000000u);
+                if (poisoned)
+#pragma unroll
+                    for (int s = 0; s < T::SEGS; ++s)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) y[s][k] = 0x7FC00000u;
             }
+            store_block<ELT, VEC>(static_cast<char*>(a.y) + (r * a.ldy + col0) * T::ES, y, valid);
+        } else {
+            // Fixed-shift-6 lift: UE8M0 code max(e + 121, 0); payload p * 2^(e + 127 - code).
+            const int code = poisoned ? 255 : max(e + 121, 0);
+            const int shift = e + 127 - code;  // 6, or 1..5 when the code is clamped at 0
+            uint32_t b[8];
+            if constexpr (ELT == Elt::BF16) {
+                // Round where the payload P reads as P * 2^(-120 + 16k): there the
+                // bf16 exponent field is the E4M3 one plus 16k, so bits 10..4 of each
+                // pattern are the E4M3 exponent and mantissa.  k keeps the
+                // multiplier 2^(7 - code + 16k) a normal bf16.
+                const int k16 = code > 133 ? ((code - 133 + 15) >> 4) << 4 : 0;
+                Bf16Grid g;
+                g.mult = bf16_pow2_pair(7 - code + k16);
+                g.floor = bf16_pow2_pair(shift - 120 + k16);
+                g.sat = g.floor + 0x01400140u;  // 6 * floor
+#pragma unroll
+                for (int s = 0; s < T::SEGS; ++s)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t w0 = v[s][2 * q], w1 = v[s][2 * q + 1];
+                        const uint32_t t0 = bf2_grid(w0 & 0x7FFF7FFFu, g), t1 = bf2_grid(w1 & 0x7FFF7FFFu, g);
+                        b[4 * s + q] = lop_select(prmt(t0 >> 4, t1 >> 4, 0x6420u), prmt(w0, w1, 0x7531u), 0x7F7F7F7Fu);
+                    }
+            } else {
+                const uint32_t mult = f32_pow2(-e), up = f32_pow2(shift);
+#pragma unroll
+                for (int s = 0; s < T::SEGS; ++s)
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t p[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t w = v[s][4 * q + i];
+                            p[i] = f32_mul(f32_grid(w & 0x7FFFFFFFu, mult), up) | (w & 0x80000000u);
+                        }
+                        b[2 * s + q] = e4m3x2_from_f32(p[1], p[0]) | (e4m3x2_from_f32(p[3], p[2]) << 16);
+                    }
+            }
+            if (poisoned)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) b[i] = 0x7F7F7F7Fu;
+            store_payload<DST>(a.data + r * a.K + col0, b, valid);
+            a.scales[scale_offset(r, j, nb, Cp, a.lay)] = (uint8_t)code;
+        }
+
+        j += step_c;
+        r += step_r;
+        if (j >= nb) {
+            j -= nb;
+            r += 1;
         }
     }
 
@@ -255,25 +253,23 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_
     }
 }
 
-template <RowMode MODE, Elt ELT, bool VEC>
+template <RowMode MODE, Elt ELT, bool VEC, int DST>
 cudaError_t launch_one(const RowwiseArgs& a, cudaStream_t s) {
-    using T = Traits<ELT>;
     const int64_t nb = (a.K + 31) / 32;
-    const int64_t cpr = nb * T::L;
-    const int64_t total = a.rows * cpr;
+    const int64_t total = a.rows * nb;
     static int occ = 0;
     if (occ == 0) {
         cudaError_t err =
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rowwise_kernel<MODE, ELT, VEC>, kThreads, 0);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rowwise_kernel<MODE, ELT, VEC, DST>, kThreads, 0);
         if (err != cudaSuccess) return err;
         if (occ < 1) occ = 1;
     }
-    int64_t grid = ceil_div(total, (int64_t)kThreads * kItems);
+    int64_t grid = ceil_div(total, (int64_t)kThreads);
     const int64_t resident = (int64_t)sm_count() * occ;
     if (grid > resident) grid = resident;
     if (grid < 1) grid = 1;
-    const int64_t stride = grid * kThreads * kItems;
-    rowwise_kernel<MODE, ELT, VEC><<<(unsigned)grid, kThreads, 0, s>>>(a, cpr, stride / cpr, stride % cpr);
+    const int64_t stride = grid * kThreads;
+    rowwise_kernel<MODE, ELT, VEC, DST><<<(unsigned)grid, kThreads, 0, s>>>(a, nb, stride / nb, stride % nb);
     return cudaGetLastError();
 }
 
@@ -282,10 +278,19 @@ bool aligned(const void* p, int64_t n) { return (reinterpret_cast<uintptr_t>(p) 
 template <RowMode MODE, Elt ELT>
 cudaError_t dispatch(const RowwiseArgs& a, cudaStream_t s) {
     using T = Traits<ELT>;
-    bool vec = aligned(a.x, 16) && (a.ldx * T::ES) % 16 == 0 && a.K % T::CH == 0;
-    if (MODE == RowMode::PROJECT) vec = vec && aligned(a.y, 16) && (a.ldy * T::ES) % 16 == 0;
-    if (MODE == RowMode::MXFP8) vec = vec && aligned(a.data, T::CH);
-    return vec ? launch_one<MODE, ELT, true>(a, s) : launch_one<MODE, ELT, false>(a, s);
+    // vector path: every 32-byte segment of the input (and projection output) is aligned
+    bool vec = aligned(a.x, 32) && (a.ldx * T::ES) % 32 == 0 && (a.K * T::ES) % 32 == 0;
+    if (MODE == RowMode::PROJECT) {
+        vec = vec && aligned(a.y, 32) && (a.ldy * T::ES) % 32 == 0;
+        return vec ? launch_one<MODE, ELT, true, 0>(a, s) : launch_one<MODE, ELT, false, 0>(a, s);
+    }
+    const int dst = (aligned(a.data, 32) && a.K % 32 == 0) ? 2 : (aligned(a.data, 16) && a.K % 16 == 0) ? 1 : 0;
+    if (vec) {
+        if (dst == 2) return launch_one<MODE, ELT, true, 2>(a, s);
+        if (dst == 1) return launch_one<MODE, ELT, true, 1>(a, s);
+        return launch_one<MODE, ELT, true, 0>(a, s);
+    }
+    return launch_one<MODE, ELT, false, 0>(a, s);
 }
 
 }  // namespace
