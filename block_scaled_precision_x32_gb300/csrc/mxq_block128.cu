@@ -98,14 +98,16 @@ __global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB)
 #pragma unroll
                 for (int s = 0; s < P::SEGS; ++s)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) m = u16x2_max(m, v[s][k] & 0x7FFF7FFFu);
+                    for (int k = 0; k < 8; ++k) m = bf2_absmax(m, v[s][k]);
+                m &= 0x7FFF7FFFu;
                 m = max(m & 0xFFFFu, m >> 16);
                 pois[i] = m >= 0x7F80u;
             } else {
 #pragma unroll
                 for (int s = 0; s < P::SEGS; ++s)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) m = max(m, v[s][k] & 0x7FFFFFFFu);
+                    for (int k = 0; k < 8; ++k) m = f32_absmax(m, v[s][k]);
+                m &= 0x7FFFFFFFu;
                 pois[i] = m >= 0x7F800000u;
             }
             eb[i] = block_exponent<P::MANT>(m);
@@ -132,22 +134,43 @@ __global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB)
             // bf16/fp32, the power-of-two fold is exact in fp32 (or far below
             // E4M3's smallest subnormal), and cvt rounds once.
             const uint32_t fold = f32_pow2(max(eb[i] - T, -126));
+            const bool top = eb[i] == 125;  // only there can |x| / 2^e round past 6
             uint32_t b[8];
             if constexpr (ELT == Elt::BF16) {
-                const Bf16Grid g = bf16_grid_unit(eb[i]);
+                if (T <= 6 && eb[i] - T >= -4) {
+                    // Every nonzero payload p * 2^(e_b - T) is >= 2^-5, an E4M3
+                    // normal, so the encode is exact: round onto the grid in the
+                    // domain z = x * 2^(-T - 120), where the bf16 exponent field of a
+                    // value equals its E4M3 one and bits 10..4 are the E4M3 byte.
+                    Bf16Grid g;
+                    g.mult = bf16_pow2_pair(-T - 120);
+                    g.floor = bf16_pow2_pair(eb[i] - T - 120);
 #pragma unroll
-                for (int s = 0; s < P::SEGS; ++s)
+                    for (int s = 0; s < P::SEGS; ++s)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t h[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const uint32_t w = v[s][2 * q + u];
-                            const uint32_t sg = bf2_grid(w & 0x7FFF7FFFu, g) | (w & 0x80008000u);
-                            h[u] = e4m3x2_from_f32(f32_mul(sg & 0xFFFF0000u, fold), f32_mul(sg << 16, fold));
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t w0 = v[s][2 * q], w1 = v[s][2 * q + 1];
+                            const uint32_t t0 = bf2_grid(w0, g), t1 = bf2_grid(w1, g);
+                            b[4 * s + q] = lop_select(prmt(t0 >> 4, t1 >> 4, 0x6420u), prmt(w0, w1, 0x7531u), 0x7F7F7F7Fu);
                         }
-                        b[4 * s + q] = h[0] | (h[1] << 16);
-                    }
+                } else {
+                    const Bf16Grid g = bf16_grid_unit(eb[i]);
+#pragma unroll
+                    for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t h[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const uint32_t w = v[s][2 * q + u];
+                                uint32_t t = bf2_grid(w, g);
+                                if (top) t = bf2_sat(t, 0x40C040C0u);
+                                const uint32_t sg = t | (w & 0x80008000u);
+                                h[u] = e4m3x2_from_f32(f32_mul(sg & 0xFFFF0000u, fold), f32_mul(sg << 16, fold));
+                            }
+                            b[4 * s + q] = h[0] | (h[1] << 16);
+                        }
+                }
             } else {
                 const uint32_t mult = f32_pow2(-eb[i]);
 #pragma unroll
@@ -158,7 +181,9 @@ __global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB)
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const uint32_t w = v[s][4 * q + u];
-                            u4[u] = f32_mul(f32_grid(w & 0x7FFFFFFFu, mult) | (w & 0x80000000u), fold);
+                            uint32_t tt = f32_grid(w, mult);
+                            if (top) tt = f32_sat(tt);
+                            u4[u] = f32_mul(tt | (w & 0x80000000u), fold);
                         }
                         b[2 * s + q] = e4m3x2_from_f32(u4[1], u4[0]) | (e4m3x2_from_f32(u4[3], u4[2]) << 16);
                     }

@@ -38,6 +38,18 @@ __device__ __forceinline__ uint32_t bf2_min(uint32_t a, uint32_t b) {
     asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
+// max(|a|, |b|) per half, NaN if either is NaN (the sign bit of the result
+// is the xor of the signs and is ignored by the callers).
+__device__ __forceinline__ uint32_t bf2_absmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t f32_absmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 __device__ __forceinline__ uint32_t u16x2_max(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -124,24 +136,31 @@ __device__ __forceinline__ int block_exponent(uint32_t amax_mag) {
 
 // ------------------------------------------------ E2M1 grid rounding, bf16
 
-// Magnitudes a (two bf16 patterns, sign cleared) of a block with exponent e
-// are scaled into v = a * 2^-e (exact: v >= 2^-126 whenever it can round to
-// a nonzero grid point) and rounded to the E2M1 grid {0, .5, 1, 1.5, 2, 3,
-// 4, 6} by one add and one subtract of c = 2^(6 + max(exp(v), 0)): the sum
-// v + c has unit in the last place 0.5 for v < 2, 1 for v in [2, 4) and 2
-// for v in [4, 8) -- the grid spacing -- and its ties go to an even
-// significand, which is the even E2M1 code.  A result of 8 (v >= 7, only
-// possible at the upper clamp e = 125) saturates to 6.
+// Elements x (two bf16 patterns, signed) of a block with exponent e are
+// scaled into v = x * 2^-e (exact whenever |v| can round to a nonzero grid
+// point: then |v| >= 2^-2 is a normal bf16) and rounded to the signed E2M1
+// grid {0, .5, 1, 1.5, 2, 3, 4, 6} by adding and subtracting
+// c = 1.5 * 2^(6 + max(exp|v|, 0)).  For |v| < 2, in [2, 4) and in [4, 8)
+// the sum v + c stays inside one binade of c whose unit in the last place
+// is 0.5, 1 and 2 -- the grid spacing there -- and c / ulp = 192 is even, so
+// round-to-nearest-even of the sum ties to the even grid multiple, which is
+// the even E2M1 code.  A result of +-8 (|v| >= 7) occurs only at the upper
+// clamp e = 125 and is saturated by the caller.  A zero result may carry the
+// wrong sign; callers OR the input's sign back in.
 struct Bf16Grid {
-    uint32_t mult;  // v = a * mult: 2^-e, or 2^-e * 2^s for a shifted domain
-    uint32_t floor; // smallest power of two allowed for c / 64: 2^0 in v units
-    uint32_t sat;   // 6 in v units
+    uint32_t mult;  // v = x * mult: 2^-e, or 2^-e * 2^s for a shifted domain
+    uint32_t floor; // 1.0 in v units (both halves)
 };
 
-__device__ __forceinline__ uint32_t bf2_grid(uint32_t a, const Bf16Grid& g) {
-    const uint32_t v = bf2_mul(a, g.mult);
-    const uint32_t c = bf2_max(v & 0x7F807F80u, g.floor) + 0x03000300u;  // * 64
-    return bf2_min(bf2_sub(bf2_add(v, c), c), g.sat);
+__device__ __forceinline__ uint32_t bf2_grid(uint32_t x, const Bf16Grid& g) {
+    const uint32_t v = bf2_mul(x, g.mult);
+    const uint32_t c = bf2_max(v & 0x7F807F80u, g.floor) + 0x03400340u;  // * 96
+    return bf2_sub(bf2_add(v, c), c);
+}
+
+// Clamp a signed grid value (in units of `one`) to [-6, 6]: sat6 = 6 * one.
+__device__ __forceinline__ uint32_t bf2_sat(uint32_t t, uint32_t sat6) {
+    return bf2_max(bf2_min(t, sat6), sat6 | 0x80008000u);
 }
 
 __device__ __forceinline__ uint32_t bf16_pow2_pair(int k) {  // 2^k, k in [-126, 127]
@@ -149,22 +168,27 @@ __device__ __forceinline__ uint32_t bf16_pow2_pair(int k) {  // 2^k, k in [-126,
     return p | (p << 16);
 }
 
-// Grid in the v = |x| / 2^e domain.
+// Grid in the v = x / 2^e domain.
 __device__ __forceinline__ Bf16Grid bf16_grid_unit(int e) {
     Bf16Grid g;
     g.mult = bf16_pow2_pair(-e);
     g.floor = 0x3F803F80u;  // 1.0
-    g.sat = 0x40C040C0u;    // 6.0
     return g;
 }
 
 // ------------------------------------------------ E2M1 grid rounding, fp32
 
-// Same construction with fp32 (c = 2^(22 + max(exp(v), 0))).
-__device__ __forceinline__ uint32_t f32_grid(uint32_t a, uint32_t mult) {
-    const uint32_t v = f32_mul(a, mult);
-    const uint32_t c = max(v & 0x7F800000u, 0x3F800000u) + (22u << 23);
-    return f32_min(f32_sub(f32_add(v, c), c), 0x40C00000u);
+// Same construction with fp32: c = 1.5 * 2^(22 + max(exp|v|, 0)).
+__device__ __forceinline__ uint32_t f32_grid(uint32_t x, uint32_t mult) {
+    const uint32_t v = f32_mul(x, mult);
+    const uint32_t c = max(v & 0x7F800000u, 0x3F800000u) + (22u << 23) + 0x00400000u;
+    return f32_sub(f32_add(v, c), c);
+}
+
+__device__ __forceinline__ uint32_t f32_sat(uint32_t t) {  // clamp to [-6, 6]
+    uint32_t d;
+    asm("{ .reg .f32 a; min.f32 a, %1, 0f40C00000; max.f32 %0, a, 0fC0C00000; }" : "=r"(d) : "r"(t));
+    return d;
 }
 
 __device__ __forceinline__ uint32_t f32_pow2(int k) {  // 2^k, k in [-127, 127]

@@ -110,23 +110,25 @@ __device__ __forceinline__ void store_payload(uint8_t* p, const uint32_t (&b)[8]
     }
 }
 
+// Largest magnitude pattern of the block; any NaN gives a NaN pattern
+// (above every finite and infinite magnitude).
 template <Elt ELT>
 __device__ __forceinline__ uint32_t block_amax(const uint32_t (&v)[Traits<ELT>::SEGS][8]) {
     using T = Traits<ELT>;
+    uint32_t m = 0u;
     if constexpr (ELT == Elt::BF16) {
-        uint32_t m = 0u;
 #pragma unroll
         for (int s = 0; s < T::SEGS; ++s)
 #pragma unroll
-            for (int k = 0; k < 8; ++k) m = u16x2_max(m, v[s][k] & 0x7FFF7FFFu);
+            for (int k = 0; k < 8; ++k) m = bf2_absmax(m, v[s][k]);
+        m &= 0x7FFF7FFFu;
         return max(m & 0xFFFFu, m >> 16);
     } else {
-        uint32_t m = 0u;
 #pragma unroll
         for (int s = 0; s < T::SEGS; ++s)
 #pragma unroll
-            for (int k = 0; k < 8; ++k) m = max(m, v[s][k] & 0x7FFFFFFFu);
-        return m;
+            for (int k = 0; k < 8; ++k) m = f32_absmax(m, v[s][k]);
+        return m & 0x7FFFFFFFu;
     }
 }
 
@@ -153,31 +155,40 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_
 
         if constexpr (MODE == RowMode::PROJECT) {
             uint32_t y[T::SEGS][8];
+            const bool top = e == 125;  // only there can |x| / 2^e round past 6
             if constexpr (ELT == Elt::BF16) {
                 const Bf16Grid g = bf16_grid_unit(e);
                 const uint32_t scl = bf16_pow2_pair(e);
 #pragma unroll
                 for (int s = 0; s < T::SEGS; ++s)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        y[s][k] = bf2_mul(bf2_grid(v[s][k] & 0x7FFF7FFFu, g), scl) | (v[s][k] & 0x80008000u);
-                if (poisoned)
+                    for (int k = 0; k < 8; ++k) y[s][k] = bf2_grid(v[s][k], g);
+                if (top)
 #pragma unroll
                     for (int s = 0; s < T::SEGS; ++s)
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) y[s][k] = 0x7FC07FC0u;
+                        for (int k = 0; k < 8; ++k) y[s][k] = bf2_sat(y[s][k], 0x40C040C0u);
+#pragma unroll
+                for (int s = 0; s < T::SEGS; ++s)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        y[s][k] = poisoned ? 0x7FC07FC0u : (bf2_mul(y[s][k], scl) | (v[s][k] & 0x80008000u));
             } else {
                 const uint32_t mult = f32_pow2(-e), scl = f32_pow2(e);
 #pragma unroll
                 for (int s = 0; s < T::SEGS; ++s)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        y[s][k] = f32_mul(f32_grid(v[s][k] & 0x7FFFFFFFu, mult), scl) | (v[s][k] & 0x80000000u);
-                if (poisoned)
+                    for (int k = 0; k < 8; ++k) y[s][k] = f32_grid(v[s][k], mult);
+                if (top)
 #pragma unroll
                     for (int s = 0; s < T::SEGS; ++s)
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) y[s][k] = 0x7FC00000u;
+                        for (int k = 0; k < 8; ++k) y[s][k] = f32_sat(y[s][k]);
+#pragma unroll
+                for (int s = 0; s < T::SEGS; ++s)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        y[s][k] = poisoned ? 0x7FC00000u : (f32_mul(y[s][k], scl) | (v[s][k] & 0x80000000u));
             }
             store_block<ELT, VEC>(static_cast<char*>(a.y) + (r * a.ldy + col0) * T::ES, y, valid);
         } else {
@@ -194,17 +205,24 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_
                 Bf16Grid g;
                 g.mult = bf16_pow2_pair(7 - code + k16);
                 g.floor = bf16_pow2_pair(shift - 120 + k16);
-                g.sat = g.floor + 0x01400140u;  // 6 * floor
+                const uint32_t sat6 = g.floor + 0x01400140u;  // 6 * floor
+                const bool top = e == 125;
 #pragma unroll
                 for (int s = 0; s < T::SEGS; ++s)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const uint32_t w0 = v[s][2 * q], w1 = v[s][2 * q + 1];
-                        const uint32_t t0 = bf2_grid(w0 & 0x7FFF7FFFu, g), t1 = bf2_grid(w1 & 0x7FFF7FFFu, g);
+                        uint32_t t0 = bf2_grid(w0, g), t1 = bf2_grid(w1, g);
+                        if (top) {
+                            t0 = bf2_sat(t0, sat6);
+                            t1 = bf2_sat(t1, sat6);
+                        }
+                        // magnitude bytes from the rounded values, sign bits from the inputs
                         b[4 * s + q] = lop_select(prmt(t0 >> 4, t1 >> 4, 0x6420u), prmt(w0, w1, 0x7531u), 0x7F7F7F7Fu);
                     }
             } else {
                 const uint32_t mult = f32_pow2(-e), up = f32_pow2(shift);
+                const bool top = e == 125;
 #pragma unroll
                 for (int s = 0; s < T::SEGS; ++s)
 #pragma unroll
@@ -213,7 +231,9 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const uint32_t w = v[s][4 * q + i];
-                            p[i] = f32_mul(f32_grid(w & 0x7FFFFFFFu, mult), up) | (w & 0x80000000u);
+                            uint32_t t = f32_grid(w, mult);
+                            if (top) t = f32_sat(t);
+                            p[i] = f32_mul(t, up) | (w & 0x80000000u);
                         }
                         b[2 * s + q] = e4m3x2_from_f32(p[1], p[0]) | (e4m3x2_from_f32(p[3], p[2]) << 16);
                     }

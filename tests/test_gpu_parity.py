@@ -327,6 +327,16 @@ def test_spread_sweep_fp32_8192(mx):
         np.testing.assert_array_equal(host_bits(bs[band]), rs.view(np.uint32)[0])
 
 
+@pytest.mark.parametrize("seed", [1004, 77])
+def test_spread_tiles_bf16(mx, seed):
+    """The spread-sweep tiles in bf16 (1024 x 1024): tiles on both sides of
+    every fast-path condition of the blockwise kernel (tile exponent above or
+    below 6, block exponents within or beyond 4 of the tile maximum), all
+    conversions against the oracle."""
+    x32, _ = syn.spread_tiles_fp32(rows=1024, K=1024, seed=seed)
+    run_all_and_compare(mx, syn.f32_to_bf16_bits(x32), layouts=(oracle.SWIZZLED,))
+
+
 def test_moe_expert_stack_export(mx):
     """32 experts x 4096 x 7184 bf16 (K % 32 = 16, 225 scale columns):
     MXFP8 rowwise into the GEMM-swizzled layout, then export; sampled
