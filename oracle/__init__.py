@@ -49,7 +49,9 @@ def _L():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # MXQ_ORACLE_LIB: load another build of the oracle source instead
+            # (the mutation tests point it at copies with planted mistakes)
+            lib = ctypes.CDLL(os.environ.get("MXQ_ORACLE_LIB") or build())
             i64, ip, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
             lib.oracle_fake_quant_mxfp4.argtypes = [vp, vp, ip, i64, i64, i64, i64]
             lib.oracle_mxfp8_row_direct.argtypes = [vp, ip, i64, i64, i64, vp, vp]

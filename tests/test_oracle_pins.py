@@ -328,6 +328,26 @@ def test_blockwise_clamp_and_planted_tiles():
     assert set(np.unique(data[:, 256:384]).tolist()) == {0x38, 0xB8}
 
 
+def test_blockwise_poisoned_block_left_out_of_tile_max():
+    """Reading of "non-finite block poisoning" for the 128x128 form: a
+    poisoned block gives payloads 0x7F and does not enter the tile maximum,
+    so the finite blocks still encode their projection exactly."""
+    x = np.zeros((128, 128), dtype=np.float32)
+    x[:, :] = np.float32(2.0 ** -50) * np.tile(np.array([6, -3, 1.5, 0.5], dtype=np.float32), 32)
+    x[5, 32:64] = np.nan
+    x[70, 0] = np.inf
+    data, sinv = oracle.fp8_block128_direct(x)
+    e_fin = oracle.block_exponent(int(np.float32(6 * 2.0 ** -50).view(np.uint32)), FP32)
+    assert sinv[0, 0] == np.float32(2.0 ** (e_fin - 6))
+    assert np.all(data[5, 32:64] == 0x7F) and np.all(data[70, 0:32] == 0x7F)
+    y = oracle.fake_quant_mxfp4(x)
+    back = oracle.dequant_block128(data, sinv, FP32)
+    finite = np.ones_like(x, dtype=bool)
+    finite[5, 32:64] = False
+    finite[70, 0:32] = False
+    np.testing.assert_array_equal(back.view(np.uint32)[finite], y.view(np.uint32)[finite])
+
+
 # ---------------------------------------------------------------- layouts
 
 def test_swizzle_offsets_golden_and_bijective():
@@ -365,8 +385,11 @@ def test_export_swizzle_invariance_and_dequant(shape):
             a = oracle.dequant_mxfp8(d, ex, oracle.COMPACT, kind, FP32)
             b = oracle.dequant_mxfp8(d, s_l, lay, kind, FP32)
             np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
-        # padding bytes are zero
         nb = -(-K // 32)
+        if lay == oracle.PADDED:  # a plain row-major (Rp, Cp) matrix
+            Rp, Cp = -(-rows_ // 128) * 128, -(-nb // 4) * 4
+            np.testing.assert_array_equal(s_l.reshape(Rp, Cp)[:rows_, :nb], s_c)
+        # padding bytes are zero
         mask = np.ones(s_l.size, dtype=bool)
         for r in range(rows_):
             for j in range(nb):
