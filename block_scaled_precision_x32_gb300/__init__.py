@@ -10,8 +10,13 @@ Functions carry the C names:
 * ``mxq_fake_quant_mxfp4``     MXFP4 projection (TE PR #3264, mode 1)
 * ``mxq_mxfp8_row_direct``     direct MXFP8 rowwise (TE PR #3264, mode 2)
 * ``mxq_fp8_block128_direct``  direct FP8 128x128 blockwise (TE PR #3264, mode 2)
-* ``mxq_dequantize``           MXFP8 rowwise / 128x128 blockwise -> bf16 / fp32
+* ``mxq_mxfp4_pack``           packed MXFP4 deployment form (TE PR #3264)
+* ``mxq_dequantize``           MXFP8 rowwise / 128x128 blockwise / packed MXFP4 -> bf16 / fp32
 * ``mxq_export_mxfp8``         export_components (TE PR #3790)
+
+The ``skip=`` argument of the converters selects the ``*_update`` entry
+points: a device int32 tensor, read when the kernel runs; nonzero means the
+call writes nothing (for cached weights inside captured CUDA graphs).
 """
 
 from __future__ import annotations
@@ -28,7 +33,7 @@ from . import build as _build
 __all__ = [
     "MXQError", "MXFP8Components", "Library", "Call", "library",
     "mxq_fake_quant_mxfp4", "mxq_mxfp8_row_direct", "mxq_fp8_block128_direct",
-    "mxq_dequantize", "mxq_export_mxfp8", "mxq_scale_bytes", "mxq_tile_scale_count",
+    "mxq_dequantize", "mxq_export_mxfp8", "mxq_mxfp4_pack", "mxq_scale_bytes", "mxq_tile_scale_count",
     "COMPACT", "PADDED", "SWIZZLED", "scale_cols",
 ]
 
@@ -37,7 +42,7 @@ _LAYOUTS = {"compact": COMPACT, "padded": PADDED, "swizzled": SWIZZLED, COMPACT:
             SWIZZLED: SWIZZLED}
 _BF16, _FP32, _FP16 = 0, 1, 2
 _E4M3, _E5M2 = 0, 1
-_MXFP8_ROW, _BLOCK128 = 0, 1
+_MXFP8_ROW, _BLOCK128, _MXFP4 = 0, 1, 2
 
 
 class MXQError(RuntimeError):
@@ -120,6 +125,12 @@ def _stream(t: torch.Tensor) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
 
+def _skip_ptr(skip: torch.Tensor) -> ctypes.c_void_p:
+    if skip.dtype != torch.int32 or skip.numel() < 1:
+        raise ValueError("skip must be a device int32 tensor (nonzero = write nothing)")
+    return ctypes.c_void_p(skip.data_ptr())
+
+
 def _need_cuda(*ts):
     for t in ts:
         if t is not None and not t.is_cuda:
@@ -142,6 +153,10 @@ class Library:
         L.mxq_fake_quant_mxfp4.argtypes = [vp, vp, ci, i64, i64, i64, i64, vp]
         L.mxq_mxfp8_row_direct.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp]
         L.mxq_fp8_block128_direct.argtypes = [vp, ci, i64, i64, i64, vp, vp, vp]
+        L.mxq_fake_quant_mxfp4_update.argtypes = [vp, vp, ci, i64, i64, i64, i64, vp, vp]
+        L.mxq_mxfp8_row_direct_update.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp, vp]
+        L.mxq_fp8_block128_direct_update.argtypes = [vp, ci, i64, i64, i64, vp, vp, vp, vp]
+        L.mxq_mxfp4_pack.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp]
         L.mxq_dequantize.argtypes = [ctypes.POINTER(_Quantized), vp, ci, vp]
         L.mxq_export_mxfp8.argtypes = [ctypes.POINTER(_Storage), vp, ctypes.c_size_t, ctypes.POINTER(_Components), vp]
         L.mxq_scale_bytes.argtypes = [i64, i64, ci]
@@ -151,7 +166,8 @@ class Library:
         L.mxq_status_string.argtypes = [ci]
         L.mxq_status_string.restype = ctypes.c_char_p
         for fn in ("mxq_fake_quant_mxfp4", "mxq_mxfp8_row_direct", "mxq_fp8_block128_direct", "mxq_dequantize",
-                   "mxq_export_mxfp8"):
+                   "mxq_export_mxfp8", "mxq_fake_quant_mxfp4_update", "mxq_mxfp8_row_direct_update",
+                   "mxq_fp8_block128_direct_update", "mxq_mxfp4_pack"):
             getattr(L, fn).restype = ci
         self.L = L
 
@@ -173,31 +189,47 @@ class Library:
     # The eager methods below are plan_*(...)() with freshly allocated
     # outputs.
 
-    def plan_fake_quant_mxfp4(self, x: torch.Tensor, out: torch.Tensor) -> "Call":
-        _need_cuda(x, out)
+    def plan_fake_quant_mxfp4(self, x: torch.Tensor, out: torch.Tensor, skip: Optional[torch.Tensor] = None) -> "Call":
+        _need_cuda(x, out, skip)
         dt = _dt_code(x)
         rows, K, ldx = _rows_view(x)
         if out.shape != x.shape or out.dtype != x.dtype:
             raise ValueError("out must match x in shape and dtype")
         _, _, ldy = _rows_view(out)
-        args = (ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(out.data_ptr()), dt, rows, K, ldx, ldy, _stream(x))
-        return Call(self, self.L.mxq_fake_quant_mxfp4, args, "mxq_fake_quant_mxfp4", (x, out), x.device)
+        args = (ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(out.data_ptr()), dt, rows, K, ldx, ldy)
+        if skip is not None:
+            args += (_skip_ptr(skip), _stream(x))
+            return Call(self, self.L.mxq_fake_quant_mxfp4_update, args, "mxq_fake_quant_mxfp4_update", (x, out, skip),
+                        x.device)
+        return Call(self, self.L.mxq_fake_quant_mxfp4, args + (_stream(x),), "mxq_fake_quant_mxfp4", (x, out), x.device)
 
-    def plan_mxfp8_row_direct(self, x: torch.Tensor, layout, data: torch.Tensor, scales: torch.Tensor) -> "Call":
-        _need_cuda(x, data, scales)
+    def _plan_rowwise_quant(self, name, x, layout, data, scales, data_bytes, skip):
+        _need_cuda(x, data, scales, skip)
         dt = _dt_code(x)
         lay = _LAYOUTS[layout]
         rows, K, ldx = _rows_view(x)
-        if not data.is_contiguous() or data.numel() != rows * K or data.dtype != torch.uint8:
-            raise ValueError("data must be a contiguous uint8 tensor of rows*K bytes")
+        if not data.is_contiguous() or data.numel() != data_bytes(rows, K) or data.dtype != torch.uint8:
+            raise ValueError("data must be a contiguous uint8 tensor of the payload size")
         if not scales.is_contiguous() or scales.dtype != torch.uint8 or scales.numel() < self.scale_bytes(rows, K, lay):
             raise ValueError("scales must be a contiguous uint8 buffer of mxq_scale_bytes() bytes")
         args = (ctypes.c_void_p(x.data_ptr()), dt, rows, K, ldx, ctypes.c_void_p(data.data_ptr()),
-                ctypes.c_void_p(scales.data_ptr()), lay, _stream(x))
-        return Call(self, self.L.mxq_mxfp8_row_direct, args, "mxq_mxfp8_row_direct", (x, data, scales), x.device)
+                ctypes.c_void_p(scales.data_ptr()), lay)
+        if skip is not None:
+            name += "_update"
+            args += (_skip_ptr(skip),)
+        return Call(self, getattr(self.L, name), args + (_stream(x),), name, (x, data, scales, skip), x.device)
 
-    def plan_fp8_block128_direct(self, x: torch.Tensor, data: torch.Tensor, tile_scale_inv: torch.Tensor) -> "Call":
-        _need_cuda(x, data, tile_scale_inv)
+    def plan_mxfp8_row_direct(self, x: torch.Tensor, layout, data: torch.Tensor, scales: torch.Tensor,
+                              skip: Optional[torch.Tensor] = None) -> "Call":
+        return self._plan_rowwise_quant("mxq_mxfp8_row_direct", x, layout, data, scales, lambda r, k: r * k, skip)
+
+    def plan_mxfp4_pack(self, x: torch.Tensor, layout, packed: torch.Tensor, scales: torch.Tensor) -> "Call":
+        return self._plan_rowwise_quant("mxq_mxfp4_pack", x, layout, packed, scales, lambda r, k: r * ((k + 1) // 2),
+                                        None)
+
+    def plan_fp8_block128_direct(self, x: torch.Tensor, data: torch.Tensor, tile_scale_inv: torch.Tensor,
+                                 skip: Optional[torch.Tensor] = None) -> "Call":
+        _need_cuda(x, data, tile_scale_inv, skip)
         dt = _dt_code(x)
         rows, K, ldx = _rows_view(x)
         if not data.is_contiguous() or data.numel() != rows * K or data.dtype != torch.uint8:
@@ -205,23 +237,38 @@ class Library:
         if tile_scale_inv.dtype != torch.float32 or tile_scale_inv.numel() < self.tile_scale_count(rows, K):
             raise ValueError("tile_scale_inv must be fp32 with ceil(rows/128)*ceil(K/128) entries")
         args = (ctypes.c_void_p(x.data_ptr()), dt, rows, K, ldx, ctypes.c_void_p(data.data_ptr()),
-                ctypes.c_void_p(tile_scale_inv.data_ptr()), _stream(x))
-        return Call(self, self.L.mxq_fp8_block128_direct, args, "mxq_fp8_block128_direct",
+                ctypes.c_void_p(tile_scale_inv.data_ptr()))
+        if skip is not None:
+            return Call(self, self.L.mxq_fp8_block128_direct_update, args + (_skip_ptr(skip), _stream(x)),
+                        "mxq_fp8_block128_direct_update", (x, data, tile_scale_inv, skip), x.device)
+        return Call(self, self.L.mxq_fp8_block128_direct, args + (_stream(x),), "mxq_fp8_block128_direct",
                     (x, data, tile_scale_inv), x.device)
 
     def plan_dequantize(self, data: torch.Tensor, out: torch.Tensor, *, scales: Optional[torch.Tensor] = None,
-                        layout="compact", fp8="e4m3", tile_scale_inv: Optional[torch.Tensor] = None) -> "Call":
+                        layout="compact", fp8="e4m3", tile_scale_inv: Optional[torch.Tensor] = None,
+                        mxfp4: bool = False) -> "Call":
+        """MXFP8 rowwise (``scales``), 128x128 (``tile_scale_inv``) or packed
+        MXFP4 (``mxfp4=True`` with ``scales``; ``data`` holds ceil(K/2) bytes
+        per row and K is taken from ``out``)."""
         _need_cuda(data, scales, tile_scale_inv, out)
-        if (scales is None) == (tile_scale_inv is None):
-            raise ValueError("pass exactly one of scales (MXFP8 rowwise) or tile_scale_inv (128x128)")
+        if (scales is None) == (tile_scale_inv is None) or (mxfp4 and scales is None):
+            raise ValueError("pass exactly one of scales (MXFP8 rowwise, MXFP4) or tile_scale_inv (128x128)")
         if not data.is_contiguous():
             raise ValueError("data must be contiguous")
-        if not out.is_contiguous() or out.shape != data.shape:
-            raise ValueError("out must be contiguous with data's shape")
-        K = data.shape[-1] if data.dim() else 1
-        rows = data.numel() // K if K else 0
+        if not out.is_contiguous():
+            raise ValueError("out must be contiguous")
+        if mxfp4:
+            K = out.shape[-1] if out.dim() else 1
+            rows = out.numel() // K if K else 0
+            if data.numel() != rows * ((K + 1) // 2):
+                raise ValueError("packed data must hold ceil(K/2) bytes per row of out")
+        else:
+            if out.shape != data.shape:
+                raise ValueError("out must have data's shape")
+            K = data.shape[-1] if data.dim() else 1
+            rows = data.numel() // K if K else 0
         q = _Quantized()
-        q.kind = _MXFP8_ROW if scales is not None else _BLOCK128
+        q.kind = _MXFP4 if mxfp4 else (_MXFP8_ROW if scales is not None else _BLOCK128)
         q.data = data.data_ptr()
         q.rows, q.K = rows, K
         q.fp8 = _fp8_code(fp8)
@@ -267,31 +314,27 @@ class Library:
 
     # -- eager conversions ----------------------------------------------
 
-    def fake_quant_mxfp4(self, x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    def fake_quant_mxfp4(self, x: torch.Tensor, out: Optional[torch.Tensor] = None,
+                         skip: Optional[torch.Tensor] = None) -> torch.Tensor:
         if out is None:
             out = torch.empty_like(x, memory_format=torch.contiguous_format)
-        self.plan_fake_quant_mxfp4(x, out)()
+        self.plan_fake_quant_mxfp4(x, out, skip)()
         return out
 
     def mxfp8_row_direct(self, x: torch.Tensor, layout="compact", data: Optional[torch.Tensor] = None,
-                         scales: Optional[torch.Tensor] = None):
+                         scales: Optional[torch.Tensor] = None, skip: Optional[torch.Tensor] = None):
         """Returns (payload uint8 of x's shape, scales).  Compact scales are
         shaped (*shape[:-1], nb); padded and swizzled ones (Rp, Cp)."""
         rows, K, _ = _rows_view(x)
-        nb = scale_cols(K)
         if data is None:
             data = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
         if scales is None:
-            if _LAYOUTS[layout] == COMPACT:
-                scales = torch.empty(tuple(x.shape[:-1]) + (nb,), dtype=torch.uint8, device=x.device)
-            else:
-                scales = torch.empty(((rows + 127) // 128 * 128, (nb + 3) // 4 * 4), dtype=torch.uint8,
-                                     device=x.device)
-        self.plan_mxfp8_row_direct(x, layout, data, scales)()
+            scales = self._scale_buffer(x, rows, K, layout)
+        self.plan_mxfp8_row_direct(x, layout, data, scales, skip)()
         return data, scales
 
     def fp8_block128_direct(self, x: torch.Tensor, data: Optional[torch.Tensor] = None,
-                            tile_scale_inv: Optional[torch.Tensor] = None):
+                            tile_scale_inv: Optional[torch.Tensor] = None, skip: Optional[torch.Tensor] = None):
         """Returns (E4M3 payload uint8 of x's shape, fp32 2^T per 128x128 tile)."""
         rows, K, _ = _rows_view(x)
         if data is None:
@@ -299,17 +342,38 @@ class Library:
         if tile_scale_inv is None:
             tile_scale_inv = torch.empty(((rows + 127) // 128, (K + 127) // 128), dtype=torch.float32,
                                          device=x.device)
-        self.plan_fp8_block128_direct(x, data, tile_scale_inv)()
+        self.plan_fp8_block128_direct(x, data, tile_scale_inv, skip)()
         return data, tile_scale_inv
+
+    def mxfp4_pack(self, x: torch.Tensor, layout="compact", packed: Optional[torch.Tensor] = None,
+                   scales: Optional[torch.Tensor] = None):
+        """Returns (nibbles uint8 (*shape[:-1], ceil(K/2)), scales) of the
+        packed MXFP4 form; scales shaped as in mxfp8_row_direct."""
+        rows, K, _ = _rows_view(x)
+        if packed is None:
+            packed = torch.empty(tuple(x.shape[:-1]) + ((K + 1) // 2,), dtype=torch.uint8, device=x.device)
+        if scales is None:
+            scales = self._scale_buffer(x, rows, K, layout)
+        self.plan_mxfp4_pack(x, layout, packed, scales)()
+        return packed, scales
+
+    def _scale_buffer(self, x, rows, K, layout):
+        nb = scale_cols(K)
+        if _LAYOUTS[layout] == COMPACT:
+            return torch.empty(tuple(x.shape[:-1]) + (nb,), dtype=torch.uint8, device=x.device)
+        return torch.empty(((rows + 127) // 128 * 128, (nb + 3) // 4 * 4), dtype=torch.uint8, device=x.device)
 
     def dequantize(self, data: torch.Tensor, *, scales: Optional[torch.Tensor] = None, layout="compact",
                    fp8="e4m3", tile_scale_inv: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
-                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
-        """MXFP8 rowwise (pass ``scales``) or 128x128 blockwise (pass
-        ``tile_scale_inv``) payload -> bf16 / fp32 of data's shape."""
+                   out: Optional[torch.Tensor] = None, mxfp4_K: Optional[int] = None) -> torch.Tensor:
+        """MXFP8 rowwise (pass ``scales``), 128x128 blockwise (pass
+        ``tile_scale_inv``) or packed MXFP4 (pass ``scales`` and ``mxfp4_K``,
+        the unpacked row length) -> bf16 / fp32."""
         if out is None:
-            out = torch.empty(data.shape, dtype=out_dtype, device=data.device)
-        self.plan_dequantize(data, out, scales=scales, layout=layout, fp8=fp8, tile_scale_inv=tile_scale_inv)()
+            shape = data.shape if mxfp4_K is None else tuple(data.shape[:-1]) + (mxfp4_K,)
+            out = torch.empty(shape, dtype=out_dtype, device=data.device)
+        self.plan_dequantize(data, out, scales=scales, layout=layout, fp8=fp8, tile_scale_inv=tile_scale_inv,
+                             mxfp4=mxfp4_K is not None)()
         return out
 
     def export_mxfp8(self, data: Optional[torch.Tensor], scales: torch.Tensor, *, shape, layout="compact",
@@ -353,16 +417,20 @@ def library() -> Library:
     return _default
 
 
-def mxq_fake_quant_mxfp4(x, out=None):
-    return library().fake_quant_mxfp4(x, out)
+def mxq_fake_quant_mxfp4(x, out=None, skip=None):
+    return library().fake_quant_mxfp4(x, out, skip)
 
 
-def mxq_mxfp8_row_direct(x, layout="compact", data=None, scales=None):
-    return library().mxfp8_row_direct(x, layout, data, scales)
+def mxq_mxfp8_row_direct(x, layout="compact", data=None, scales=None, skip=None):
+    return library().mxfp8_row_direct(x, layout, data, scales, skip)
 
 
-def mxq_fp8_block128_direct(x, data=None, tile_scale_inv=None):
-    return library().fp8_block128_direct(x, data, tile_scale_inv)
+def mxq_fp8_block128_direct(x, data=None, tile_scale_inv=None, skip=None):
+    return library().fp8_block128_direct(x, data, tile_scale_inv, skip)
+
+
+def mxq_mxfp4_pack(x, layout="compact", packed=None, scales=None):
+    return library().mxfp4_pack(x, layout, packed, scales)
 
 
 def mxq_dequantize(data, **kw):

@@ -69,14 +69,15 @@ size_t mxq_tile_scale_count(int64_t rows, int64_t K) {
     return (size_t)(((rows + 127) / 128) * ((K + 127) / 128));
 }
 
-mxq_status mxq_fake_quant_mxfp4(const void* x, void* y, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
-                                int64_t ldy, cudaStream_t stream) {
+mxq_status mxq_fake_quant_mxfp4_update(const void* x, void* y, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                       int64_t ldy, const int32_t* skip, cudaStream_t stream) {
     mxq_status st = check_dtype(dt);
     if (st != MXQ_OK) return st;
     if (!valid_shape(rows, K, ldx) || !valid_shape(rows, K, ldy)) return MXQ_ERR_INVALID_ARG;
     if (rows == 0 || K == 0) return MXQ_OK;
     if (!x || !y || !aligned(x, elt_size(dt)) || !aligned(y, elt_size(dt))) return MXQ_ERR_INVALID_ARG;
     if (x == y && ldx != ldy) return MXQ_ERR_INVALID_ARG;
+    if (skip && !aligned(skip, 4)) return MXQ_ERR_INVALID_ARG;
     mxq::RowwiseArgs a{};
     a.x = x;
     a.y = y;
@@ -84,16 +85,24 @@ mxq_status mxq_fake_quant_mxfp4(const void* x, void* y, mxq_dtype dt, int64_t ro
     a.K = K;
     a.ldx = ldx;
     a.ldy = ldy;
+    a.skip = skip;
     return launch_status(mxq::launch_rowwise(mxq::RowMode::PROJECT, elt_of(dt), a, stream));
 }
 
-mxq_status mxq_mxfp8_row_direct(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* data,
-                                uint8_t* scales, mxq_scale_layout lay, cudaStream_t stream) {
+mxq_status mxq_fake_quant_mxfp4(const void* x, void* y, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                int64_t ldy, cudaStream_t stream) {
+    return mxq_fake_quant_mxfp4_update(x, y, dt, rows, K, ldx, ldy, nullptr, stream);
+}
+
+static mxq_status rowwise_quant(mxq::RowMode mode, const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                uint8_t* data, uint8_t* scales, mxq_scale_layout lay, const int32_t* skip,
+                                cudaStream_t stream) {
     mxq_status st = check_dtype(dt);
     if (st != MXQ_OK) return st;
     if (!valid_shape(rows, K, ldx) || !valid_layout(lay)) return MXQ_ERR_INVALID_ARG;
     if (rows == 0 || K == 0) return MXQ_OK;
     if (!x || !data || !scales || !aligned(x, elt_size(dt))) return MXQ_ERR_INVALID_ARG;
+    if (skip && !aligned(skip, 4)) return MXQ_ERR_INVALID_ARG;
     mxq::RowwiseArgs a{};
     a.x = x;
     a.data = data;
@@ -103,17 +112,36 @@ mxq_status mxq_mxfp8_row_direct(const void* x, mxq_dtype dt, int64_t rows, int64
     a.ldx = ldx;
     a.ldy = K;
     a.lay = (int)lay;
-    return launch_status(mxq::launch_rowwise(mxq::RowMode::MXFP8, elt_of(dt), a, stream));
+    a.skip = skip;
+    return launch_status(mxq::launch_rowwise(mode, elt_of(dt), a, stream));
 }
 
-mxq_status mxq_fp8_block128_direct(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* data,
-                                   float* tile_scale_inv, cudaStream_t stream) {
+mxq_status mxq_mxfp8_row_direct_update(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                       uint8_t* data, uint8_t* scales, mxq_scale_layout lay, const int32_t* skip,
+                                       cudaStream_t stream) {
+    return rowwise_quant(mxq::RowMode::MXFP8, x, dt, rows, K, ldx, data, scales, lay, skip, stream);
+}
+
+mxq_status mxq_mxfp8_row_direct(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* data,
+                                uint8_t* scales, mxq_scale_layout lay, cudaStream_t stream) {
+    return rowwise_quant(mxq::RowMode::MXFP8, x, dt, rows, K, ldx, data, scales, lay, nullptr, stream);
+}
+
+mxq_status mxq_mxfp4_pack(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* packed,
+                          uint8_t* scales, mxq_scale_layout lay, cudaStream_t stream) {
+    return rowwise_quant(mxq::RowMode::MXFP4, x, dt, rows, K, ldx, packed, scales, lay, nullptr, stream);
+}
+
+mxq_status mxq_fp8_block128_direct_update(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                          uint8_t* data, float* tile_scale_inv, const int32_t* skip,
+                                          cudaStream_t stream) {
     mxq_status st = check_dtype(dt);
     if (st != MXQ_OK) return st;
     if (!valid_shape(rows, K, ldx)) return MXQ_ERR_INVALID_ARG;
     if (rows == 0 || K == 0) return MXQ_OK;
     if (!x || !data || !tile_scale_inv || !aligned(x, elt_size(dt)) || !aligned(tile_scale_inv, 4))
         return MXQ_ERR_INVALID_ARG;
+    if (skip && !aligned(skip, 4)) return MXQ_ERR_INVALID_ARG;
     mxq::Block128Args a{};
     a.x = x;
     a.data = data;
@@ -121,7 +149,13 @@ mxq_status mxq_fp8_block128_direct(const void* x, mxq_dtype dt, int64_t rows, in
     a.rows = rows;
     a.K = K;
     a.ldx = ldx;
+    a.skip = skip;
     return launch_status(mxq::launch_block128(elt_of(dt), a, stream));
+}
+
+mxq_status mxq_fp8_block128_direct(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* data,
+                                   float* tile_scale_inv, cudaStream_t stream) {
+    return mxq_fp8_block128_direct_update(x, dt, rows, K, ldx, data, tile_scale_inv, nullptr, stream);
 }
 
 mxq_status mxq_dequantize(const mxq_quantized* q, void* out, mxq_dtype out_dt, cudaStream_t stream) {
@@ -129,13 +163,14 @@ mxq_status mxq_dequantize(const mxq_quantized* q, void* out, mxq_dtype out_dt, c
     mxq_status st = check_dtype(out_dt);
     if (st != MXQ_OK) return st;
     if (!valid_shape(q->rows, q->K, q->K)) return MXQ_ERR_INVALID_ARG;
-    if (q->kind != MXQ_QUANT_MXFP8_ROW && q->kind != MXQ_QUANT_FP8_BLOCK128) return MXQ_ERR_INVALID_ARG;
-    if (q->fp8 != MXQ_E4M3 && q->fp8 != MXQ_E5M2) return MXQ_ERR_INVALID_ARG;
+    if (q->kind != MXQ_QUANT_MXFP8_ROW && q->kind != MXQ_QUANT_FP8_BLOCK128 && q->kind != MXQ_QUANT_MXFP4)
+        return MXQ_ERR_INVALID_ARG;
+    if (q->kind != MXQ_QUANT_MXFP4 && q->fp8 != MXQ_E4M3 && q->fp8 != MXQ_E5M2) return MXQ_ERR_INVALID_ARG;
     if (q->kind == MXQ_QUANT_FP8_BLOCK128 && q->fp8 != MXQ_E4M3) return MXQ_ERR_INVALID_ARG;
-    if (q->kind == MXQ_QUANT_MXFP8_ROW && !valid_layout(q->lay)) return MXQ_ERR_INVALID_ARG;
+    if (q->kind != MXQ_QUANT_FP8_BLOCK128 && !valid_layout(q->lay)) return MXQ_ERR_INVALID_ARG;
     if (q->rows == 0 || q->K == 0) return MXQ_OK;
     if (!q->data || !out || !aligned(out, elt_size(out_dt))) return MXQ_ERR_INVALID_ARG;
-    if (q->kind == MXQ_QUANT_MXFP8_ROW && !q->scales) return MXQ_ERR_INVALID_ARG;
+    if (q->kind != MXQ_QUANT_FP8_BLOCK128 && !q->scales) return MXQ_ERR_INVALID_ARG;
     if (q->kind == MXQ_QUANT_FP8_BLOCK128 && (!q->tile_scale_inv || !aligned(q->tile_scale_inv, 4)))
         return MXQ_ERR_INVALID_ARG;
     mxq::DequantArgs a{};

@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB)
     __shared__ int warp_max[P::NT / 32];
     const int t = threadIdx.x;
     const int64_t tj = blockIdx.x;
+    if (a.skip != nullptr && *a.skip != 0) return;  // skip-update request: write nothing
 
     for (int64_t ti = blockIdx.y; ti < tiles_r; ti += gridDim.y) {
         const char* xp[P::BPL];

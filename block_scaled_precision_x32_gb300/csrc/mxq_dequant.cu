@@ -19,7 +19,9 @@
 // E5M2).  Blocks with a NaN or Inf payload, scale code 255, or a smaller
 // code for fp32 output take the element-wise fp32 path, which also makes
 // NaN canonical.  The 128x128 form multiplies by an arbitrary fp32
-// scale_inv and always takes the fp32 path.
+// scale_inv and always takes the fp32 path.  Packed MXFP4 (16 bytes of
+// nibbles per block) decodes each E2M1 value exactly in fp32 and scales it
+// by 2^(code-127) (exact, or Inf past fp32's range).
 #include <cuda_runtime.h>
 
 #include "mxq_device.cuh"
@@ -132,6 +134,40 @@ __device__ __forceinline__ void store_out(void* out, const uint32_t* o, int vali
     }
 }
 
+// Signed E2M1 nibble -> fp32 pattern of its value.
+__device__ __forceinline__ uint32_t e2m1_f32(uint32_t nib) {
+    const uint32_t m = nib & 7u;
+    const uint32_t mag = m >= 2u ? 0x3F000000u + (m << 22) : (m ? 0x3F000000u : 0u);  // 1, 1.5, 2, 3, 4, 6 / 0.5 / 0
+    return mag | ((nib & 8u) << 28);
+}
+
+template <int SRC>
+__device__ __forceinline__ void load_nibbles(uint32_t (&w)[4], const uint8_t* p, int valid) {
+    const int nbytes = (valid + 1) >> 1;
+    if constexpr (SRC == 2) {
+        const uint4 a = *reinterpret_cast<const uint4*>(p);
+        w[0] = a.x;
+        w[1] = a.y;
+        w[2] = a.z;
+        w[3] = a.w;
+    } else if constexpr (SRC == 1) {
+        const uint2 a = *reinterpret_cast<const uint2*>(p);
+        w[0] = a.x;
+        w[1] = a.y;
+        w[2] = w[3] = 0u;
+        if (nbytes > 8) {
+            const uint2 b = *reinterpret_cast<const uint2*>(p + 8);
+            w[2] = b.x;
+            w[3] = b.y;
+        }
+    } else {
+        w[0] = w[1] = w[2] = w[3] = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i < nbytes) w[i >> 2] |= (uint32_t)p[i] << ((i & 3) * 8);
+    }
+}
+
 template <int KIND, bool E5M2, bool BF16OUT, int SRC, bool VOUT>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a, int64_t nb, int64_t step_r,
                                                            int64_t step_c) {
@@ -146,6 +182,34 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a, int64_
     for (int64_t wi = tid; wi < total; wi += S) {
         const int64_t col0 = j * 32;
         const int valid = (int)min((int64_t)32, a.K - col0);
+        if constexpr (KIND == 2) {
+            uint32_t w[4];
+            load_nibbles<SRC>(w, a.data + r * ((a.K + 1) >> 1) + j * 16, valid);
+            const uint32_t c = a.scales[scale_offset(r, j, nb, Cp, a.lay)];
+            const uint32_t scale32 = c == 255u ? 0x7FC00000u : f32_pow2((int)c - 127);
+            uint32_t o[WORDS];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                uint32_t f = f32_mul(e2m1_f32((w[i >> 3] >> ((i & 7) * 4)) & 15u), scale32);
+                if ((f & 0x7FFFFFFFu) > 0x7F800000u) f = 0x7FC00000u;
+                if constexpr (BF16OUT) {
+                    if (i & 1)
+                        o[i >> 1] |= bf16_rne(f) << 16;
+                    else
+                        o[i >> 1] = bf16_rne(f);
+                } else {
+                    o[i] = f;
+                }
+            }
+            store_out<BF16OUT, VOUT>(static_cast<char*>(a.out) + (r * a.K + col0) * (BF16OUT ? 2 : 4), o, valid);
+            j += step_c;
+            r += step_r;
+            if (j >= nb) {
+                j -= nb;
+                r += 1;
+            }
+            continue;
+        }
         uint32_t w[8];
         load_payload<SRC>(w, a.data + r * a.K + col0, valid);
         uint32_t scale32;  // fp32 multiplier of the element-wise path
@@ -230,7 +294,9 @@ bool aligned(const void* p, int64_t n) { return (reinterpret_cast<uintptr_t>(p) 
 
 template <int KIND, bool E5M2, bool BF16OUT>
 cudaError_t pick_paths(const DequantArgs& a, cudaStream_t s) {
-    const int src = (aligned(a.data, 32) && a.K % 32 == 0) ? 2 : (aligned(a.data, 16) && a.K % 16 == 0) ? 1 : 0;
+    // payload bytes per block: 32 (fp8) or 16 (packed MXFP4)
+    const int src = KIND == 2 ? ((aligned(a.data, 16) && a.K % 32 == 0) ? 2 : (aligned(a.data, 8) && a.K % 16 == 0) ? 1 : 0)
+                              : ((aligned(a.data, 32) && a.K % 32 == 0) ? 2 : (aligned(a.data, 16) && a.K % 16 == 0) ? 1 : 0);
     const int es = BF16OUT ? 2 : 4;
     const bool vout = aligned(a.out, 32) && (a.K * es) % 32 == 0;
     if (src == 2) return vout ? launch_one<KIND, E5M2, BF16OUT, 2, true>(a, s) : launch_one<KIND, E5M2, BF16OUT, 2, false>(a, s);
@@ -249,6 +315,7 @@ cudaError_t pick_formats(const DequantArgs& a, cudaStream_t s) {
 
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s) {
     if (a.kind == 0) return pick_formats<0>(a, s);
+    if (a.kind == 2) return a.out_bf16 ? pick_paths<2, false, true>(a, s) : pick_paths<2, false, false>(a, s);
     // the 128x128 form carries E4M3 payloads only (checked by the caller)
     return a.out_bf16 ? pick_paths<1, false, true>(a, s) : pick_paths<1, false, false>(a, s);
 }

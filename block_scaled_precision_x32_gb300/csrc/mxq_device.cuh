@@ -82,6 +82,13 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(uint32_t hi, uint32_t lo) {
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "r"(hi), "r"(lo));
     return d;
 }
+// Two fp32 values -> two E2M1 codes (round to nearest even, saturating at
+// +-6, sign in bit 3); `hi` goes to bits 7..4, `lo` to bits 3..0.
+__device__ __forceinline__ uint32_t e2m1x2_from_f32(uint32_t hi, uint32_t lo) {
+    uint32_t d;
+    asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(d) : "r"(hi), "r"(lo));
+    return d;
+}
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -125,13 +132,14 @@ __device__ __forceinline__ uint32_t lop_select(uint32_t a, uint32_t b, uint32_t 
 // finite amax (TE PR #3264 "MXFP4 weight QAT on MXFP8 and FP8 block-scaling
 // recipes", Description, mode 1).  amax = (1 + f) * 2^E gives E - 2 when
 // f <= 1/2, else E - 1; zero and subnormal amax clamp to -126.
-template <int MANT>
+// The packed MXFP4 form keeps the rule but clamps above at 126 (TOP).
+template <int MANT, int TOP = 125>
 __device__ __forceinline__ int block_exponent(uint32_t amax_mag) {
     const int E = (int)(amax_mag >> MANT);
     const uint32_t frac = amax_mag & ((1u << MANT) - 1u);
     int e = E - 129 + (frac > (1u << (MANT - 1)) ? 1 : 0);
     e = E == 0 ? -126 : e;
-    return min(max(e, -126), 125);
+    return min(max(e, -126), TOP);
 }
 
 // ------------------------------------------------ E2M1 grid rounding, bf16

@@ -9,15 +9,16 @@
 namespace mxq {
 
 enum class Elt { BF16, FP32 };
-enum class RowMode { PROJECT, MXFP8 };
+enum class RowMode { PROJECT, MXFP8, MXFP4 };
 
 struct RowwiseArgs {
     const void* x;
     void* y;          // PROJECT output
-    uint8_t* data;    // MXFP8 payload [rows, K]
-    uint8_t* scales;  // MXFP8 scale bytes in `lay`
+    uint8_t* data;    // MXFP8 payload [rows, K]; MXFP4 nibbles [rows, ceil(K/2)]
+    uint8_t* scales;  // UE8M0 scale bytes in `lay`
     int64_t rows, K, ldx, ldy;
     int lay;          // mxq_scale_layout
+    const int32_t* skip;  // optional device flag: nonzero = write nothing
 };
 
 struct Block128Args {
@@ -25,10 +26,11 @@ struct Block128Args {
     uint8_t* data;
     float* tile_scale_inv;
     int64_t rows, K, ldx;
+    const int32_t* skip;  // optional device flag: nonzero = write nothing
 };
 
 struct DequantArgs {
-    int kind;  // mxq_quant_kind
+    int kind;  // mxq_quant_kind (0 MXFP8 row, 1 128x128, 2 packed MXFP4)
     const uint8_t* data;
     int64_t rows, K;
     int fp8;   // mxq_fp8

@@ -1,8 +1,9 @@
-// mxq_rowwise.cu -- the two 1x32-block kernels: MXFP4 projection and the
-// direct MXFP4 -> MXFP8 rowwise conversion.
+// mxq_rowwise.cu -- the 1x32-block kernels: MXFP4 projection, the direct
+// MXFP4 -> MXFP8 rowwise conversion and the packed MXFP4 deployment form.
 //
 // TE PR #3264 "MXFP4 weight QAT on MXFP8 and FP8 block-scaling recipes",
-// Description, mode 1 (projection) and mode 2 (direct, MXFP8 rowwise).
+// Description, mode 1 (projection) and mode 2 (direct, MXFP8 rowwise);
+// "Known limitations" (packed deployment's scale 2^126 past the cap).
 //
 // Work split.  Each lane owns whole 1x32 blocks: it reads a block as two
 // (bf16) or four (fp32) 32-byte vectors -- one full sector each, so a warp's
@@ -112,6 +113,23 @@ __device__ __forceinline__ void store_payload(uint8_t* p, const uint32_t (&b)[8]
 
 // Largest magnitude pattern of the block; any NaN gives a NaN pattern
 // (above every finite and infinite magnitude).
+// 16 bytes of nibbles (32 elements; valid of them present).  DST 2: one
+// 16-byte store, 1: 8-byte stores, 0: bytes.
+template <int DST>
+__device__ __forceinline__ void store_nibbles(uint8_t* p, const uint32_t (&n)[4], int valid) {
+    const int nbytes = (valid + 1) >> 1;
+    if constexpr (DST == 2) {
+        st16(p, n[0], n[1], n[2], n[3]);
+    } else if constexpr (DST == 1) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(n[0], n[1]);
+        if (nbytes > 8) *reinterpret_cast<uint2*>(p + 8) = make_uint2(n[2], n[3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i < nbytes) p[i] = (uint8_t)(n[i >> 2] >> ((i & 3) * 8));
+    }
+}
+
 template <Elt ELT>
 __device__ __forceinline__ uint32_t block_amax(const uint32_t (&v)[Traits<ELT>::SEGS][8]) {
     using T = Traits<ELT>;
@@ -140,6 +158,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_
     const int64_t S = (int64_t)gridDim.x * kThreads;
     const int64_t total = a.rows * nb;
     const int64_t Cp = (nb + 3) & ~int64_t(3);
+    if (a.skip != nullptr && *a.skip != 0) return;  // skip-update request: write nothing
     int64_t r = tid / nb, j = tid - (tid / nb) * nb;
 
     for (int64_t w = tid; w < total; w += S) {
@@ -151,7 +170,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_
 
         const uint32_t amax = block_amax<ELT>(v);
         const bool poisoned = amax >= (ELT == Elt::BF16 ? 0x7F80u : 0x7F800000u);
-        const int e = block_exponent<T::MANT>(amax);
+        const int e = block_exponent<T::MANT, MODE == RowMode::MXFP4 ? 126 : 125>(amax);
 
         if constexpr (MODE == RowMode::PROJECT) {
             uint32_t y[T::SEGS][8];
@@ -191,6 +210,29 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_
                         y[s][k] = poisoned ? 0x7FC00000u : (f32_mul(y[s][k], scl) | (v[s][k] & 0x80000000u));
             }
             store_block<ELT, VEC>(static_cast<char*>(a.y) + (r * a.ldy + col0) * T::ES, y, valid);
+        } else if constexpr (MODE == RowMode::MXFP4) {
+            // E2M1 codes of x / 2^e by the hardware conversion (round to nearest
+            // even; |x| / 2^e <= 6 by the choice of e, so nothing saturates).
+            const uint32_t mult = f32_pow2(-e);
+            uint32_t n[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int s = 0; s < T::SEGS; ++s)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if constexpr (ELT == Elt::BF16) {
+                        const uint32_t w = v[s][k];
+                        const int i = s * 8 + k;  // byte i holds elements 2i, 2i+1
+                        n[i >> 2] |= e2m1x2_from_f32(f32_mul(w & 0xFFFF0000u, mult), f32_mul(w << 16, mult))
+                                     << ((i & 3) * 8);
+                    } else if ((k & 1) == 0) {
+                        const int i = (s * 8 + k) >> 1;
+                        n[i >> 2] |= e2m1x2_from_f32(f32_mul(v[s][k + 1], mult), f32_mul(v[s][k], mult))
+                                     << ((i & 3) * 8);
+                    }
+                }
+            if (poisoned) n[0] = n[1] = n[2] = n[3] = 0u;
+            store_nibbles<DST>(a.data + r * ((a.K + 1) >> 1) + j * 16, n, valid);
+            a.scales[scale_offset(r, j, nb, Cp, a.lay)] = (uint8_t)(poisoned ? 255 : e + 127);
         } else {
             // Fixed-shift-6 lift: UE8M0 code max(e + 121, 0); payload p * 2^(e + 127 - code).
             const int code = poisoned ? 255 : max(e + 121, 0);
@@ -253,7 +295,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_
         }
     }
 
-    if (MODE == RowMode::MXFP8 && a.lay != 0) {
+    if (MODE != RowMode::PROJECT && a.lay != 0) {
         // zero the padding of the padded / swizzled scale buffer
         const int64_t Rp = (a.rows + 127) & ~int64_t(127);
         const int64_t extra = Cp - nb;
@@ -300,9 +342,19 @@ cudaError_t dispatch(const RowwiseArgs& a, cudaStream_t s) {
     using T = Traits<ELT>;
     // vector path: every 32-byte segment of the input (and projection output) is aligned
     bool vec = aligned(a.x, 32) && (a.ldx * T::ES) % 32 == 0 && (a.K * T::ES) % 32 == 0;
-    if (MODE == RowMode::PROJECT) {
+    if constexpr (MODE == RowMode::PROJECT) {
         vec = vec && aligned(a.y, 32) && (a.ldy * T::ES) % 32 == 0;
         return vec ? launch_one<MODE, ELT, true, 0>(a, s) : launch_one<MODE, ELT, false, 0>(a, s);
+    }
+    if constexpr (MODE == RowMode::MXFP4) {
+        // nibble rows are ceil(K/2) bytes: 16-byte stores need K % 32 == 0, 8-byte ones K % 16 == 0
+        const int dst = (aligned(a.data, 16) && a.K % 32 == 0) ? 2 : (aligned(a.data, 8) && a.K % 16 == 0) ? 1 : 0;
+        if (vec) {
+            if (dst == 2) return launch_one<MODE, ELT, true, 2>(a, s);
+            if (dst == 1) return launch_one<MODE, ELT, true, 1>(a, s);
+            return launch_one<MODE, ELT, true, 0>(a, s);
+        }
+        return launch_one<MODE, ELT, false, 0>(a, s);
     }
     const int dst = (aligned(a.data, 32) && a.K % 32 == 0) ? 2 : (aligned(a.data, 16) && a.K % 16 == 0) ? 1 : 0;
     if (vec) {
@@ -319,6 +371,8 @@ cudaError_t launch_rowwise(RowMode mode, Elt elt, const RowwiseArgs& a, cudaStre
     if (mode == RowMode::PROJECT)
         return elt == Elt::BF16 ? dispatch<RowMode::PROJECT, Elt::BF16>(a, s)
                                 : dispatch<RowMode::PROJECT, Elt::FP32>(a, s);
+    if (mode == RowMode::MXFP4)
+        return elt == Elt::BF16 ? dispatch<RowMode::MXFP4, Elt::BF16>(a, s) : dispatch<RowMode::MXFP4, Elt::FP32>(a, s);
     return elt == Elt::BF16 ? dispatch<RowMode::MXFP8, Elt::BF16>(a, s) : dispatch<RowMode::MXFP8, Elt::FP32>(a, s);
 }
 

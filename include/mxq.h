@@ -139,15 +139,49 @@ MXQ_API mxq_status mxq_mxfp8_row_direct(const void* x, mxq_dtype dt, int64_t row
 MXQ_API mxq_status mxq_fp8_block128_direct(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* data,
                                    float* tile_scale_inv, cudaStream_t stream);
 
-typedef enum { MXQ_QUANT_MXFP8_ROW = 0, MXQ_QUANT_FP8_BLOCK128 = 1 } mxq_quant_kind;
+/* Packed MXFP4, the deployment form of the projection (TE PR #3264,
+ * Description: training sees exactly the deployment weight, E2M1 payloads
+ * with 1x32 power-of-two UE8M0 scales; "Known limitations": above
+ * amax = 6*2^125 packed deployment moves to the scale 2^126).
+ * Block exponent e' = clamp(ceil(log2(amax/6)), -126, 126) -- the
+ * projection's rule with the upper clamp at 126 -- stored as the UE8M0 code
+ * e' + 127; each element is the E2M1 code nearest |x|/2^e' (ties to the even
+ * code) with the sign in bit 3.  Element 2i is the low nibble of byte i of
+ * its row, element 2i+1 the high nibble (a missing last element leaves 0).
+ * Wherever amax <= 6*2^125 the packed weight decodes exactly to
+ * mxq_fake_quant_mxfp4's output.  A poisoned block has scale code 0xFF and
+ * zero nibbles.
+ *   x:      [rows, ldx] bf16 or fp32.
+ *   packed: [rows, ceil(K/2)] bytes, contiguous.
+ *   scales: mxq_scale_bytes(rows, K, lay) bytes in layout `lay`.
+ * Errors: as mxq_mxfp8_row_direct. */
+MXQ_API mxq_status mxq_mxfp4_pack(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* packed,
+                                  uint8_t* scales, mxq_scale_layout lay, cudaStream_t stream);
+
+/* Skip-update variants of the converters, for cached weights updated inside
+ * a captured CUDA graph (TE PR #3264, review: a direct cache-hit update must
+ * honour the skip-update flag of CUDA-graph replays).  `skip` is a device
+ * int32 read when the kernel runs; if it is nonzero the call writes nothing
+ * (every output keeps its previous bytes).  skip == NULL behaves as the
+ * plain entry point.  Arguments and errors otherwise as above. */
+MXQ_API mxq_status mxq_fake_quant_mxfp4_update(const void* x, void* y, mxq_dtype dt, int64_t rows, int64_t K,
+                                               int64_t ldx, int64_t ldy, const int32_t* skip, cudaStream_t stream);
+MXQ_API mxq_status mxq_mxfp8_row_direct_update(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                               uint8_t* data, uint8_t* scales, mxq_scale_layout lay,
+                                               const int32_t* skip, cudaStream_t stream);
+MXQ_API mxq_status mxq_fp8_block128_direct_update(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                                  uint8_t* data, float* tile_scale_inv, const int32_t* skip,
+                                                  cudaStream_t stream);
+
+typedef enum { MXQ_QUANT_MXFP8_ROW = 0, MXQ_QUANT_FP8_BLOCK128 = 1, MXQ_QUANT_MXFP4 = 2 } mxq_quant_kind;
 
 /* A quantized tensor of rows x K as read by mxq_dequantize. */
 typedef struct {
     mxq_quant_kind kind;
-    const uint8_t* data;         /* [rows, K] payload bytes, contiguous */
+    const uint8_t* data;         /* [rows, K] payload bytes, contiguous; MXFP4: [rows, ceil(K/2)] nibbles */
     int64_t rows, K;
-    mxq_fp8 fp8;                 /* payload encoding; BLOCK128 takes E4M3 only */
-    const uint8_t* scales;       /* MXFP8_ROW: UE8M0 codes in layout `lay` */
+    mxq_fp8 fp8;                 /* payload encoding; BLOCK128 takes E4M3 only; MXFP4 ignores it */
+    const uint8_t* scales;       /* MXFP8_ROW, MXFP4: UE8M0 codes in layout `lay` */
     mxq_scale_layout lay;
     const float* tile_scale_inv; /* FP8_BLOCK128: [ceil(rows/128), ceil(K/128)] */
 } mxq_quantized;
@@ -156,8 +190,9 @@ typedef struct {
  * (the export decodes to dequantize() exactly); TE PR #3264, Description
  * (UE8M0 decode: code 0 is 2^-127, code 255 is NaN).
  * MXFP8_ROW: out = payload * 2^(code - 127); BLOCK128: out = payload *
- * tile_scale_inv.  fp32 output is that product rounded to nearest even
- * (exact for power-of-two scales, Inf on overflow); bf16 output is one more
+ * tile_scale_inv; MXFP4: out = E2M1 value * 2^(code - 127).  fp32 output is
+ * that product rounded to nearest even (exact for power-of-two scales, Inf
+ * on overflow, e.g. 4 * 2^126); bf16 output is one more
  * round-to-nearest-even of the fp32 value.
  *   out: [rows, K] contiguous, dtype out_dt (fp16 rejected).
  * Errors: INVALID_ARG, UNSUPPORTED_DTYPE. */

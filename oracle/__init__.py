@@ -74,6 +74,10 @@ def _L():
             lib.oracle_e4m3_rtne.restype = ctypes.c_uint8
             lib.oracle_e8m0_value.argtypes = [ctypes.c_uint8]
             lib.oracle_e8m0_value.restype = ctypes.c_double
+            lib.oracle_mxfp4_pack.argtypes = [vp, ip, i64, i64, i64, vp, vp]
+            lib.oracle_dequant_mxfp4.argtypes = [vp, vp, ip, i64, i64, vp, ip]
+            lib.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_value.restype = ctypes.c_double
             lib.oracle_f32_to_bf16.argtypes = [ctypes.c_uint32]
             lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
             _lib = lib
@@ -182,6 +186,34 @@ def dequant_block128(data: np.ndarray, tile_scale_inv: np.ndarray, out_dt: int) 
     if data.size:
         _L().oracle_dequant_block128(_ptr(data), _ptr(sinv), rows, K, _ptr(out), out_dt)
     return out
+
+
+def mxfp4_pack(x: np.ndarray, lay: int = COMPACT):
+    """Packed MXFP4: (nibbles uint8 [rows, ceil(K/2)], scales in ``lay``)."""
+    dt = _dt_of(x)
+    rows, K, ldx = _rows_k_ld(x)
+    packed = np.zeros((rows, (K + 1) // 2), dtype=np.uint8)
+    nb = scale_cols(K)
+    compact = np.empty((rows, nb), dtype=np.uint8)
+    if x.size:
+        _L().oracle_mxfp4_pack(_ptr(x), dt, rows, K, ldx, _ptr(packed), _ptr(compact))
+    if lay == COMPACT:
+        return packed, compact
+    return packed, scales_to_layout(compact, rows, K, lay)
+
+
+def dequant_mxfp4(packed: np.ndarray, scales: np.ndarray, lay: int, K: int, out_dt: int) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows = packed.shape[0] if packed.ndim > 1 else 1
+    out = np.empty((rows, K), dtype=np.float32 if out_dt == FP32 else np.uint16)
+    if rows and K:
+        _L().oracle_dequant_mxfp4(_ptr(packed), _ptr(scales), lay, rows, K, _ptr(out), out_dt)
+    return out
+
+
+def e2m1_value(nibble: int) -> float:
+    return float(_L().oracle_e2m1_value(nibble))
 
 
 def export_scales(scales: np.ndarray, lay: int, rows: int, K: int) -> np.ndarray:

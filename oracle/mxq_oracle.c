@@ -148,24 +148,25 @@ static uint32_t canonical_nan(int dt) { return dt == OR_BF16 ? 0x7FC0u : 0x7FC00
 
 /* ------------------------------------------------------ MXFP4 decomposition */
 
-/* Block scale exponent from the amax bit pattern (TE PR #3264, Description,
- * mode 1): e = clamp(ceil(log2(amax/6)), -126, 125).
+/* ceil(log2(amax/6)) from the amax bit pattern (TE PR #3264, Description,
+ * mode 1: the scale is "derived from the amax bit pattern").
  *
  * With amax = (1 + m/2^M) * 2^E normal, amax/6 lies in
  * [2^(E-2)/1.5, 2^(E-1)/1.5), so ceil(log2(amax/6)) = E - 2 when
  * 1 + m/2^M <= 1.5 and E - 1 otherwise.  A zero or subnormal amax sits below
- * 6*2^-129, so the clamp gives -126. */
-static int block_exponent(uint32_t amax_mag_bits, int dt) {
+ * 6*2^-129; it is returned as -1000, below every clamp. */
+static int ceil_log2_amax_over_6(uint32_t amax_mag_bits, int dt) {
     ieee_fmt f = fmt_of(dt);
     uint32_t m = amax_mag_bits & ((1u << f.mant_bits) - 1u);
     int E = (int)(amax_mag_bits >> f.mant_bits);
-    int e;
-    if (E == 0) {
-        e = -126;
-    } else {
-        uint32_t half = 1u << (f.mant_bits - 1);
-        e = (E - f.bias) - 2 + (m > half ? 1 : 0);
-    }
+    if (E == 0) return -1000;
+    uint32_t half = 1u << (f.mant_bits - 1);
+    return (E - f.bias) - 2 + (m > half ? 1 : 0);
+}
+
+/* Block scale exponent of the projection: clamp(ceil(log2(amax/6)), -126, 125). */
+static int block_exponent(uint32_t amax_mag_bits, int dt) {
+    int e = ceil_log2_amax_over_6(amax_mag_bits, dt);
     if (e < -126) e = -126;
     if (e > 125) e = 125;
     return e;
@@ -484,6 +485,75 @@ int oracle_dequant_block128(const uint8_t* data, const float* tile_scale_inv, in
         for (int64_t i = 0; i < K; ++i) {
             double prod = oracle_fp8_value(data[r * K + i], OR_E4M3) * (double)tile_scale_inv[(r / 128) * tc + i / 128];
             store_result(out, out_dt, r * K + i, prod);
+        }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------ packed MXFP4 */
+
+/* Packed MXFP4 deployment form (TE PR #3264, Description: training sees
+ * exactly the deployment weight, E2M1 payloads with 1x32 power-of-two
+ * UE8M0 scales; "Known limitations": above amax = 6*2^125 packed deployment
+ * moves to the scale 2^126, which bf16/fp32 cannot materialise).  Reading:
+ * the block exponent is clamp(ceil(log2(amax/6)), -126, 126) -- the
+ * projection's rule with the upper clamp at 126 -- its UE8M0 code is
+ * e + 127, and each element is the E2M1 code nearest |x|/2^e (ties to the
+ * even code) with the sign in bit 3.  Element 2i sits in the low nibble of
+ * byte i of the row, element 2i+1 in the high nibble; a missing last
+ * element leaves a zero nibble.  A poisoned block has scale code 0xFF and
+ * zero nibbles.  packed is [rows, ceil(K/2)], scales compact [rows, nb]. */
+int oracle_mxfp4_pack(const void* x, int dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* packed,
+                      uint8_t* scales) {
+    if (dt != OR_BF16 && dt != OR_FP32) return OR_BAD;
+    size_t es = dt == OR_BF16 ? 2 : 4;
+    int64_t nb = oracle_scale_cols(K), pb = (K + 1) / 2;
+    for (int64_t r = 0; r < rows; ++r) {
+        const char* xr = (const char*)x + (size_t)(r * ldx) * es;
+        memset(packed + r * pb, 0, (size_t)pb);
+        for (int64_t j0 = 0; j0 < K; j0 += 32) {
+            int64_t j1 = j0 + 32 < K ? j0 + 32 : K;
+            block_info b = scan_block(xr, dt, j0, j1);
+            if (b.poisoned) {
+                scales[r * nb + j0 / 32] = 0xFF;
+                continue;
+            }
+            uint32_t amax = 0;
+            for (int64_t i = j0; i < j1; ++i) {
+                uint32_t mag = magnitude_bits(load_bits(xr, dt, i), dt);
+                if (mag > amax) amax = mag;
+            }
+            /* the projection's rule with the upper clamp moved to 126 */
+            int e = ceil_log2_amax_over_6(amax, dt);
+            if (e < -126) e = -126;
+            if (e > 126) e = 126;
+            scales[r * nb + j0 / 32] = (uint8_t)(e + 127);
+            for (int64_t i = j0; i < j1; ++i) {
+                uint32_t bits = load_bits(xr, dt, i);
+                int c = element_code(bits, dt, e) | (sign_of(bits, dt) << 3);
+                packed[r * pb + i / 2] |= (uint8_t)(c << ((i % 2) * 4));
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* Value of a signed E2M1 nibble. */
+double oracle_e2m1_value(uint8_t nibble) {
+    double v = E2M1_GRID[nibble & 7];
+    return (nibble & 8) ? -v : v;
+}
+
+/* Packed MXFP4 -> fp32 / bf16: out = value(nibble) * 2^(code-127), rounded
+ * to nearest in fp32 (exact, or Inf where 2^126 * 4 or more overflows),
+ * then to bf16.  scales are in layout lay. */
+int oracle_dequant_mxfp4(const uint8_t* packed, const uint8_t* scales, int lay, int64_t rows, int64_t K, void* out,
+                         int out_dt) {
+    int64_t nb = oracle_scale_cols(K), pb = (K + 1) / 2;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t i = 0; i < K; ++i) {
+            uint8_t c = scales[oracle_scale_offset(r, i / 32, nb, lay)];
+            uint8_t nib = (uint8_t)((packed[r * pb + i / 2] >> ((i % 2) * 4)) & 15);
+            store_result(out, out_dt, r * K + i, oracle_e2m1_value(nib) * oracle_e8m0_value(c));
         }
     return OR_OK;
 }

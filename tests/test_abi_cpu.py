@@ -121,6 +121,19 @@ def test_host_side_rejections(libs):
     q.fp8 = 1
     assert L.mxq_dequantize(ctypes.byref(q), FAKE, 0, None) == INVALID  # blockwise is E4M3 only
     assert L.mxq_dequantize(None, FAKE, 0, None) == INVALID
+    # skip flags must be int32-aligned device pointers; packed MXFP4 validates like MXFP8
+    L.mxq_mxfp8_row_direct_update.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                              ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                              ctypes.c_void_p, ctypes.c_void_p]
+    assert L.mxq_mxfp8_row_direct_update(FAKE, 0, 4, 32, 32, FAKE, FAKE, 0, FAKE + 2, None) == INVALID
+    assert L.mxq_mxfp8_row_direct_update(FAKE, 2, 4, 32, 32, FAKE, FAKE, 0, FAKE, None) == UNSUPPORTED
+    L.mxq_mxfp4_pack.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    assert L.mxq_mxfp4_pack(FAKE, 2, 4, 32, 32, FAKE, FAKE, 0, None) == UNSUPPORTED
+    assert L.mxq_mxfp4_pack(FAKE, 0, 4, 32, 32, FAKE, FAKE, 7, None) == INVALID
+    assert L.mxq_mxfp4_pack(None, 0, 0, 32, 32, None, None, 0, None) == OK
+    q = _Q(kind=2, data=FAKE, rows=4, K=32, fp8=9, scales=None, lay=0, tile_scale_inv=None)
+    assert L.mxq_dequantize(ctypes.byref(q), FAKE, 0, None) == INVALID  # MXFP4 needs scales
 
 
 def test_export_host_logic(libs):

@@ -75,6 +75,25 @@ def run_all_and_compare(mx, x_np, layouts=LAYOUTS, block128=True, guard=True):
                 np.testing.assert_array_equal(host_bits(a), want)
                 np.testing.assert_array_equal(host_bits(b), want)  # export decodes to dequantize()
 
+    # packed MXFP4 (deployment form), each scale layout, and its dequantize
+    ref_p, ref_pc = oracle.mxfp4_pack(x_np, oracle.COMPACT)
+    for lay in layouts:
+        nbytes = mx.scale_bytes(rows, K, lay)
+        p = Guarded((rows, (K + 1) // 2), torch.uint8)
+        s = Guarded((max(nbytes, 1),), torch.uint8)
+        x2 = x if x.dim() == 2 else x.reshape(rows, K)
+        mx.mxfp4_pack(x2, lay, packed=p.t, scales=s.t)
+        torch.cuda.synchronize()
+        assert p.intact() and s.intact()
+        np.testing.assert_array_equal(host_bits(p.t), ref_p)
+        ref_lay = ref_pc.reshape(-1) if lay == oracle.COMPACT else oracle.scales_to_layout(ref_pc, rows, K, lay)
+        np.testing.assert_array_equal(host_bits(s.t)[:nbytes], ref_lay)
+        for odt, ocode in ((torch.float32, oracle.FP32), (torch.bfloat16, oracle.BF16)):
+            got = mx.dequantize(p.t, scales=s.t[:nbytes], layout=lay, out_dtype=odt, mxfp4_K=K)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(host_bits(got).reshape(rows, K),
+                                          oracle_bits(oracle.dequant_mxfp4(ref_p, ref_pc, oracle.COMPACT, K, ocode)))
+
     if block128:
         ref_d, ref_s = oracle.fp8_block128_direct(x_np)
         d = Guarded(x.shape, torch.uint8)
@@ -367,6 +386,101 @@ def test_moe_expert_stack_export(mx):
         np.testing.assert_array_equal(host_bits(comp.scale_inv[e][rows]), rs)
 
 
+# ------------------------------------------------------ skip-update flag
+
+def test_skip_flag_leaves_every_output_untouched(mx):
+    """A nonzero device flag makes the *_update converters write nothing --
+    payloads, scales (padding included) and tile scales keep their bytes."""
+    x = dev_bf16(syn.normal_bf16(256, 512, seed=31))
+    skip = torch.ones(1, dtype=torch.int32, device="cuda")
+    y = torch.full((256, 512), 1.0, dtype=torch.bfloat16, device="cuda")
+    d = torch.full((256, 512), 0x5A, dtype=torch.uint8, device="cuda")
+    s = torch.full((mx.scale_bytes(256, 512, "swizzled"),), 0x5A, dtype=torch.uint8, device="cuda")
+    bd = torch.full((256, 512), 0x5A, dtype=torch.uint8, device="cuda")
+    bs = torch.full((mx.tile_scale_count(256, 512),), 3.0, dtype=torch.float32, device="cuda")
+    mx.fake_quant_mxfp4(x, out=y, skip=skip)
+    mx.mxfp8_row_direct(x, "swizzled", data=d, scales=s, skip=skip)
+    mx.fp8_block128_direct(x, data=bd, tile_scale_inv=bs, skip=skip)
+    torch.cuda.synchronize()
+    assert bool((y == 1.0).all()) and bool((d == 0x5A).all()) and bool((s == 0x5A).all())
+    assert bool((bd == 0x5A).all()) and bool((bs == 3.0).all())
+    skip.zero_()
+    mx.fake_quant_mxfp4(x, out=y, skip=skip)
+    mx.mxfp8_row_direct(x, "swizzled", data=d, scales=s, skip=skip)
+    mx.fp8_block128_direct(x, data=bd, tile_scale_inv=bs, skip=skip)
+    ry = mx.fake_quant_mxfp4(x)
+    rd, rs = mx.mxfp8_row_direct(x, "swizzled")
+    rbd, rbs = mx.fp8_block128_direct(x)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), ry.view(torch.int16))
+    assert torch.equal(d, rd) and torch.equal(s, rs.reshape(-1))
+    assert torch.equal(bd, rbd) and torch.equal(bs.view(torch.int32), rbs.reshape(-1).view(torch.int32))
+
+
+def test_skip_flag_in_a_captured_graph(mx):
+    """The flag is read at replay: a graph captured once refreshes the cached
+    MXFP8 weight when the flag is 0 and keeps it when it is 1 (TE PR #3264,
+    review: skipped cached updates during CUDA-graph replay)."""
+    x1 = syn.normal_bf16(384, 1024, seed=41)
+    x2 = syn.normal_bf16(384, 1024, seed=42)
+    x = dev_bf16(x1)
+    skip = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = torch.empty((384, 1024), dtype=torch.uint8, device="cuda")
+    s = torch.empty(mx.scale_bytes(384, 1024, "swizzled"), dtype=torch.uint8, device="cuda")
+    bd = torch.empty((384, 1024), dtype=torch.uint8, device="cuda")
+    bs = torch.empty(mx.tile_scale_count(384, 1024), dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        calls = [mx.plan_mxfp8_row_direct(x, "swizzled", d, s, skip=skip), mx.plan_fp8_block128_direct(x, bd, bs, skip=skip)]
+        for c in calls:
+            c()
+        side.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for c in calls:
+                c()
+    torch.cuda.current_stream().wait_stream(side)
+
+    def want(xn):
+        rd, rs = oracle.mxfp8_row_direct(xn, oracle.SWIZZLED)
+        bdd, bss = oracle.fp8_block128_direct(xn)
+        return rd, rs, bdd, bss.view(np.uint32).reshape(-1)
+
+    g.replay()
+    torch.cuda.synchronize()
+    w1 = want(x1)
+    for got, ref in zip((d, s, bd, bs), w1):
+        np.testing.assert_array_equal(host_bits(got), ref)
+    x.copy_(dev_bf16(x2))
+    skip.fill_(1)
+    g.replay()
+    torch.cuda.synchronize()
+    for got, ref in zip((d, s, bd, bs), w1):  # kept
+        np.testing.assert_array_equal(host_bits(got), ref)
+    skip.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for got, ref in zip((d, s, bd, bs), want(x2)):  # refreshed
+        np.testing.assert_array_equal(host_bits(got), ref)
+
+
+def test_packed_mxfp4_moe_expert_sampled(mx):
+    """Packed MXFP4 of one 4096 x 7184 expert (K % 32 = 16, 225 scale
+    columns) in the swizzled layout; sampled rows against the oracle."""
+    xe = syn.moe_expert_bf16(7)
+    x = dev_bf16(xe)
+    p, s = mx.mxfp4_pack(x, "swizzled")
+    pc, sc = mx.mxfp4_pack(x, "compact")
+    comp = mx.export_mxfp8(torch.empty(x.shape, dtype=torch.uint8, device="cuda"), s, shape=x.shape, layout="swizzled")
+    torch.cuda.synchronize()
+    assert torch.equal(p, pc) and torch.equal(comp.scale_inv, sc)
+    rows = _sample_rows(4096, 16, 7)
+    rp, rs = oracle.mxfp4_pack(xe[rows])
+    np.testing.assert_array_equal(host_bits(p[rows]), rp)
+    np.testing.assert_array_equal(host_bits(sc[rows]), rs)
+
+
 # ------------------------------------------------------- fast-math build
 
 def test_fast_math_build_gives_identical_bytes(mx):
@@ -392,3 +506,9 @@ def test_fast_math_build_gives_identical_bytes(mx):
             da, sa = lib_a.fp8_block128_direct(x)
             db, sb = lib_b.fp8_block128_direct(x)
             assert torch.equal(da, db) and torch.equal(sa.view(torch.int32), sb.view(torch.int32))
+            pa, qa = lib_a.mxfp4_pack(x, "swizzled")
+            pb, qb = lib_b.mxfp4_pack(x, "swizzled")
+            assert torch.equal(pa, pb) and torch.equal(qa, qb)
+            K = x.shape[-1]
+            assert torch.equal(lib_a.dequantize(pa, scales=qa, layout="swizzled", mxfp4_K=K).view(torch.int16),
+                               lib_b.dequantize(pb, scales=qb, layout="swizzled", mxfp4_K=K).view(torch.int16))

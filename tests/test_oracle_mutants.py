@@ -20,9 +20,11 @@ SRC = os.path.join(ROOT, "oracle", "mxq_oracle.c")
 
 MUTANTS = {
     "scale rule: >= at the 1.5 boundary": ("(m > half ? 1 : 0)", "(m >= half ? 1 : 0)"),
-    "scale rule: dropped -1": ("e = (E - f.bias) - 2 + (m > half ? 1 : 0);", "e = (E - f.bias) - 1 + (m > half ? 1 : 0);"),
-    "scale rule: lower clamp -127": ("    if (e < -126) e = -126;\n", "    if (e < -127) e = -127;\n"),
-    "scale rule: upper clamp 126": ("    if (e > 125) e = 125;\n", "    if (e > 126) e = 126;\n"),
+    "scale rule: dropped -1": ("return (E - f.bias) - 2 + (m > half ? 1 : 0);", "return (E - f.bias) - 1 + (m > half ? 1 : 0);"),
+    "scale rule: lower clamp -127": ("    if (e < -126) e = -126;\n    if (e > 125) e = 125;", "    if (e < -127) e = -127;\n    if (e > 125) e = 125;"),
+    "scale rule: upper clamp 126": ("    if (e > 125) e = 125;\n", "    if (e > 125) e = 126;\n"),
+    "packed MXFP4: upper clamp 125": ("            if (e > 126) e = 126;\n", "            if (e > 125) e = 125;\n"),
+    "packed MXFP4: high nibble first": ("(uint8_t)(c << ((i % 2) * 4))", "(uint8_t)(c << ((1 - i % 2) * 4))"),
     "E2M1 ties to odd": ("if (dc < db || (dc == db && (c % 2) == 0)) best = c;\n    }\n    return best;\n}\n\ntypedef",
                          "if (dc < db || (dc == db && (c % 2) == 1)) best = c;\n    }\n    return best;\n}\n\ntypedef"),
     "E2M1 grid point 6 -> 5": ("{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}", "{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 5.0}"),

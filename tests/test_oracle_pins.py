@@ -348,6 +348,63 @@ def test_blockwise_poisoned_block_left_out_of_tile_max():
     np.testing.assert_array_equal(back.view(np.uint32)[finite], y.view(np.uint32)[finite])
 
 
+# ------------------------------------------------------ packed MXFP4
+
+def test_packed_mxfp4_decodes_to_projection_and_moves_past_the_cap():
+    """The packed deployment form decodes exactly to the projection wherever
+    amax <= 6*2^125; above it the scale moves to 2^126 and the nibbles are
+    the nearest grid points of |x|/2^126 (TE PR #3264, Description and
+    "Known limitations")."""
+    from fractions import Fraction
+    g = kv("mxfp4_packed_saturation.txt")
+    x = syn.exhaustive_bf16()
+    packed, scales = oracle.mxfp4_pack(x)
+    y = oracle.fake_quant_mxfp4(x)
+    back = oracle.dequant_mxfp4(packed, scales, oracle.COMPACT, 32, BF16)
+    mag = x & 0x7FFF
+    poisoned = np.any(mag >= 0x7F80, axis=1)
+    over = np.any((mag > 0x7F40) & (mag < 0x7F80), axis=1) & ~poisoned
+    ok = ~poisoned & ~over
+    assert int(ok.sum()) == 2036
+    np.testing.assert_array_equal(back[ok], y[ok])
+    assert np.all(scales[poisoned, 0] == 0xFF) and np.all(packed[poisoned] == 0)
+    assert np.all(scales[over, 0] == int(g["saturating_scale_code"]))
+    # nibbles of the saturating rows: nearest grid point of |x| / 2^126, ties to even
+    for r in np.nonzero(over)[0]:
+        for i in range(32):
+            v = Fraction(bf.bf16_to_float(int(x[r, i])))
+            a = abs(v) / Fraction(2) ** 126
+            c = min(range(8), key=lambda k: (abs(a - bf.GRID[k]), k % 2))
+            nib = (int(packed[r, i // 2]) >> ((i % 2) * 4)) & 15
+            assert nib == (c | (8 if v < 0 or (v == 0 and x[r, i] & 0x8000) else 0)), (r, i)
+    # the projection instead holds those rows at the cap 2^125 * 6 (scale code 252)
+    _, row_scales = oracle.mxfp8_row_direct(x[over])
+    assert np.all(row_scales[:, 0] + 6 == int(g["projection_cap_scale_code"]))
+
+
+def test_packed_mxfp4_nibble_order_and_partial_blocks():
+    """Element 2i in the low nibble, 2i+1 in the high nibble; a short last
+    block keeps its own scale (K = 48 -> 24 bytes, 2 scales)."""
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, :4] = [0.5, 6.0, -1.0, 3.0]  # amax 6 -> e = 0, codes 1, 7, 8|2, 5
+    packed, scales = oracle.mxfp4_pack(x)
+    assert scales[0, 0] == 127
+    assert packed[0, 0] == 0x71 and packed[0, 1] == 0x5A
+    for shape in ((100, 48), (64, 16)):
+        xx = syn.partial_block_fp32(shape)
+        packed, scales = oracle.mxfp4_pack(xx)
+        assert packed.shape == (shape[0], shape[1] // 2) and scales.shape == (shape[0], -(-shape[1] // 32))
+        back = oracle.dequant_mxfp4(packed, scales, oracle.COMPACT, shape[1], FP32)
+        np.testing.assert_array_equal(back.view(np.uint32), oracle.fake_quant_mxfp4(xx).view(np.uint32))
+
+
+def test_e2m1_nibble_values():
+    vals = [oracle.e2m1_value(n) for n in range(16)]
+    assert vals[:8] == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert vals[8:] == [-0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+    assert math.copysign(1.0, vals[8]) == -1.0
+
+
 # ---------------------------------------------------------------- layouts
 
 def test_swizzle_offsets_golden_and_bijective():
