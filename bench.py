@@ -53,8 +53,17 @@ KERNEL_FILES = {
     "block128": "mxq_block128.cu",
     "dequant_bf16": "mxq_dequant.cu",
     "export": "mxq_export.cu",
+    "mxfp8_col": "mxq_colwise.cu",
+    "mxfp4_pack": "mxq_rowwise.cu",
+    "mxfp4_dequant_bf16": "mxq_dequant.cu",
 }
 STEP_BYTES = sum(BYTES.values())
+# Conversions beyond the five of the step, timed alone the same way.
+EXTRA_BYTES = {
+    "mxfp8_col": 2 * N + N + N // 32,
+    "mxfp4_pack": 2 * N + N // 2 + N // 32,
+    "mxfp4_dequant_bf16": N // 2 + N // 32 + 2 * N,
+}
 CSRC = os.path.join(ROOT, "block_scaled_precision_x32_gb300", "csrc")
 
 
@@ -163,9 +172,16 @@ def run_gpu(args, rank, world):
         dq_in.append((d, s))
     dq_out = torch.empty_like(x0)
     ex_out = torch.empty(ROWS * NB, dtype=torch.uint8, device=dev)
+    p4 = torch.empty((ROWS, COLS // 2), dtype=torch.uint8, device=dev)
+    p4_s = torch.empty(lib.scale_bytes(ROWS, COLS, "swizzled"), dtype=torch.uint8, device=dev)
+    p4_in = [lib.mxfp4_pack(xs[i], "swizzled") for i in range(R)]
+    p4_out = torch.empty_like(x0)
+    col_d = torch.empty_like(row_d)
+    col_s = torch.empty(lib.scale_bytes(COLS, ROWS, "swizzled"), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
     names = list(BYTES)
+    extra = list(EXTRA_BYTES)
     # Prepared calls (arguments marshalled once), made on a side stream and
     # captured into CUDA graphs: one graph per input rotation holding the
     # step's five launches, and per conversion one graph of R back-to-back
@@ -184,8 +200,12 @@ def run_gpu(args, rank, world):
                 lib.plan_dequantize(dq_d, dq_out, scales=dq_s, layout="swizzled"),
                 lib.plan_export_mxfp8(dq_d, dq_s, shape=(ROWS, COLS), layout="swizzled", scale_out=ex_out)[0],
             ])
+        extra_plans = [[lib.plan_mxfp8_col_direct(xs[s], "swizzled", col_d, col_s),
+                        lib.plan_mxfp4_pack(xs[s], "swizzled", p4, p4_s),
+                        lib.plan_dequantize(p4_in[s][0], p4_out, scales=p4_in[s][1], layout="swizzled", mxfp4=True)]
+                       for s in range(R)]
         for s in range(2 * R):  # warm every launch configuration before capture
-            for c in plans[s % R]:
+            for c in plans[s % R] + extra_plans[s % R]:
                 c()
         side.synchronize()
         step_graphs, conv_graphs = [], []
@@ -200,6 +220,12 @@ def run_gpu(args, rank, world):
             with torch.cuda.graph(g, stream=side):
                 for s in range(R):
                     plans[s][i]()
+            conv_graphs.append(g)
+        for i in range(len(extra)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for s in range(R):
+                    extra_plans[s][i]()
             conv_graphs.append(g)
     torch.cuda.current_stream(dev).wait_stream(side)
     torch.cuda.synchronize()
@@ -225,7 +251,7 @@ def run_gpu(args, rank, world):
     # timed region 2: each conversion alone, R * ceil(steps / R) launches back to back
     reps = max(1, -(-args.steps // R))
     per = {}
-    for i, nm in enumerate(names):
+    for i, nm in enumerate(names + extra):
         conv_graphs[i].replay()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
@@ -243,11 +269,12 @@ def run_gpu(args, rank, world):
         return None
     peak, peak_src = load_peaks()
     per_conv = {}
-    for nm in names:
+    for nm in names + extra:
+        nbytes = BYTES.get(nm, EXTRA_BYTES.get(nm))
         us = per[nm] * 1e3
-        gbs = BYTES[nm] / (us * 1e-6) / 1e9
-        per_conv[nm] = {"us": round(us, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
-                        "bytes": BYTES[nm]}
+        gbs = nbytes / (us * 1e-6) / 1e9
+        per_conv[nm] = {"us": round(us, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nbytes,
+                        "in_step": nm in BYTES}
     dom = max(names, key=lambda nm: per_conv[nm]["us"])
     traffic = load_traffic()
     value = world * STEP_BYTES / (ms_step * 1e-3) / 1e9

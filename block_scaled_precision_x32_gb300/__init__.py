@@ -11,6 +11,7 @@ Functions carry the C names:
 * ``mxq_mxfp8_row_direct``     direct MXFP8 rowwise (TE PR #3264, mode 2)
 * ``mxq_fp8_block128_direct``  direct FP8 128x128 blockwise (TE PR #3264, mode 2)
 * ``mxq_mxfp4_pack``           packed MXFP4 deployment form (TE PR #3264)
+* ``mxq_mxfp8_col_direct``     direct MXFP8 columnwise, 32x1 blocks (TE PR #3264, mode 2)
 * ``mxq_dequantize``           MXFP8 rowwise / 128x128 blockwise / packed MXFP4 -> bf16 / fp32
 * ``mxq_export_mxfp8``         export_components (TE PR #3790)
 
@@ -33,7 +34,8 @@ from . import build as _build
 __all__ = [
     "MXQError", "MXFP8Components", "Library", "Call", "library",
     "mxq_fake_quant_mxfp4", "mxq_mxfp8_row_direct", "mxq_fp8_block128_direct",
-    "mxq_dequantize", "mxq_export_mxfp8", "mxq_mxfp4_pack", "mxq_scale_bytes", "mxq_tile_scale_count",
+    "mxq_dequantize", "mxq_export_mxfp8", "mxq_mxfp4_pack", "mxq_mxfp8_col_direct", "mxq_scale_bytes",
+    "mxq_tile_scale_count",
     "COMPACT", "PADDED", "SWIZZLED", "scale_cols",
 ]
 
@@ -42,7 +44,7 @@ _LAYOUTS = {"compact": COMPACT, "padded": PADDED, "swizzled": SWIZZLED, COMPACT:
             SWIZZLED: SWIZZLED}
 _BF16, _FP32, _FP16 = 0, 1, 2
 _E4M3, _E5M2 = 0, 1
-_MXFP8_ROW, _BLOCK128, _MXFP4 = 0, 1, 2
+_MXFP8_ROW, _BLOCK128, _MXFP4, _MXFP8_COL = 0, 1, 2, 3
 
 
 class MXQError(RuntimeError):
@@ -157,6 +159,7 @@ class Library:
         L.mxq_mxfp8_row_direct_update.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp, vp]
         L.mxq_fp8_block128_direct_update.argtypes = [vp, ci, i64, i64, i64, vp, vp, vp, vp]
         L.mxq_mxfp4_pack.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp]
+        L.mxq_mxfp8_col_direct.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp]
         L.mxq_dequantize.argtypes = [ctypes.POINTER(_Quantized), vp, ci, vp]
         L.mxq_export_mxfp8.argtypes = [ctypes.POINTER(_Storage), vp, ctypes.c_size_t, ctypes.POINTER(_Components), vp]
         L.mxq_scale_bytes.argtypes = [i64, i64, ci]
@@ -167,7 +170,7 @@ class Library:
         L.mxq_status_string.restype = ctypes.c_char_p
         for fn in ("mxq_fake_quant_mxfp4", "mxq_mxfp8_row_direct", "mxq_fp8_block128_direct", "mxq_dequantize",
                    "mxq_export_mxfp8", "mxq_fake_quant_mxfp4_update", "mxq_mxfp8_row_direct_update",
-                   "mxq_fp8_block128_direct_update", "mxq_mxfp4_pack"):
+                   "mxq_fp8_block128_direct_update", "mxq_mxfp4_pack", "mxq_mxfp8_col_direct"):
             getattr(L, fn).restype = ci
         self.L = L
 
@@ -227,6 +230,21 @@ class Library:
         return self._plan_rowwise_quant("mxq_mxfp4_pack", x, layout, packed, scales, lambda r, k: r * ((k + 1) // 2),
                                         None)
 
+    def plan_mxfp8_col_direct(self, x: torch.Tensor, layout, data: torch.Tensor, scales: torch.Tensor) -> "Call":
+        """Columnwise MXFP8: data [rows, K]; scales hold the K x ceil(rows/32)
+        scale matrix of the transposed tensor in ``layout``."""
+        _need_cuda(x, data, scales)
+        dt = _dt_code(x)
+        lay = _LAYOUTS[layout]
+        rows, K, ldx = _rows_view(x)
+        if not data.is_contiguous() or data.numel() != rows * K or data.dtype != torch.uint8:
+            raise ValueError("data must be a contiguous uint8 tensor of rows*K bytes")
+        if not scales.is_contiguous() or scales.dtype != torch.uint8 or scales.numel() < self.scale_bytes(K, rows, lay):
+            raise ValueError("scales must be a contiguous uint8 buffer of mxq_scale_bytes(K, rows) bytes")
+        args = (ctypes.c_void_p(x.data_ptr()), dt, rows, K, ldx, ctypes.c_void_p(data.data_ptr()),
+                ctypes.c_void_p(scales.data_ptr()), lay, _stream(x))
+        return Call(self, self.L.mxq_mxfp8_col_direct, args, "mxq_mxfp8_col_direct", (x, data, scales), x.device)
+
     def plan_fp8_block128_direct(self, x: torch.Tensor, data: torch.Tensor, tile_scale_inv: torch.Tensor,
                                  skip: Optional[torch.Tensor] = None) -> "Call":
         _need_cuda(x, data, tile_scale_inv, skip)
@@ -246,7 +264,7 @@ class Library:
 
     def plan_dequantize(self, data: torch.Tensor, out: torch.Tensor, *, scales: Optional[torch.Tensor] = None,
                         layout="compact", fp8="e4m3", tile_scale_inv: Optional[torch.Tensor] = None,
-                        mxfp4: bool = False) -> "Call":
+                        mxfp4: bool = False, columnwise: bool = False) -> "Call":
         """MXFP8 rowwise (``scales``), 128x128 (``tile_scale_inv``) or packed
         MXFP4 (``mxfp4=True`` with ``scales``; ``data`` holds ceil(K/2) bytes
         per row and K is taken from ``out``)."""
@@ -268,7 +286,7 @@ class Library:
             K = data.shape[-1] if data.dim() else 1
             rows = data.numel() // K if K else 0
         q = _Quantized()
-        q.kind = _MXFP4 if mxfp4 else (_MXFP8_ROW if scales is not None else _BLOCK128)
+        q.kind = _MXFP4 if mxfp4 else (_MXFP8_COL if columnwise else (_MXFP8_ROW if scales is not None else _BLOCK128))
         q.data = data.data_ptr()
         q.rows, q.K = rows, K
         q.fp8 = _fp8_code(fp8)
@@ -345,6 +363,22 @@ class Library:
         self.plan_fp8_block128_direct(x, data, tile_scale_inv, skip)()
         return data, tile_scale_inv
 
+    def mxfp8_col_direct(self, x: torch.Tensor, layout="compact", data: Optional[torch.Tensor] = None,
+                         scales: Optional[torch.Tensor] = None):
+        """Returns (payload uint8 [rows, K], scales of the K x ceil(rows/32)
+        transposed scale matrix: compact (K, nbr), padded/swizzled (Kp, Cp))."""
+        rows, K, _ = _rows_view(x)
+        nbr = (rows + 31) // 32
+        if data is None:
+            data = torch.empty((rows, K), dtype=torch.uint8, device=x.device)
+        if scales is None:
+            if _LAYOUTS[layout] == COMPACT:
+                scales = torch.empty((K, nbr), dtype=torch.uint8, device=x.device)
+            else:
+                scales = torch.empty(((K + 127) // 128 * 128, (nbr + 3) // 4 * 4), dtype=torch.uint8, device=x.device)
+        self.plan_mxfp8_col_direct(x, layout, data, scales)()
+        return data, scales
+
     def mxfp4_pack(self, x: torch.Tensor, layout="compact", packed: Optional[torch.Tensor] = None,
                    scales: Optional[torch.Tensor] = None):
         """Returns (nibbles uint8 (*shape[:-1], ceil(K/2)), scales) of the
@@ -365,7 +399,8 @@ class Library:
 
     def dequantize(self, data: torch.Tensor, *, scales: Optional[torch.Tensor] = None, layout="compact",
                    fp8="e4m3", tile_scale_inv: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
-                   out: Optional[torch.Tensor] = None, mxfp4_K: Optional[int] = None) -> torch.Tensor:
+                   out: Optional[torch.Tensor] = None, mxfp4_K: Optional[int] = None,
+                   columnwise: bool = False) -> torch.Tensor:
         """MXFP8 rowwise (pass ``scales``), 128x128 blockwise (pass
         ``tile_scale_inv``) or packed MXFP4 (pass ``scales`` and ``mxfp4_K``,
         the unpacked row length) -> bf16 / fp32."""
@@ -373,7 +408,7 @@ class Library:
             shape = data.shape if mxfp4_K is None else tuple(data.shape[:-1]) + (mxfp4_K,)
             out = torch.empty(shape, dtype=out_dtype, device=data.device)
         self.plan_dequantize(data, out, scales=scales, layout=layout, fp8=fp8, tile_scale_inv=tile_scale_inv,
-                             mxfp4=mxfp4_K is not None)()
+                             mxfp4=mxfp4_K is not None, columnwise=columnwise)()
         return out
 
     def export_mxfp8(self, data: Optional[torch.Tensor], scales: torch.Tensor, *, shape, layout="compact",
@@ -427,6 +462,10 @@ def mxq_mxfp8_row_direct(x, layout="compact", data=None, scales=None, skip=None)
 
 def mxq_fp8_block128_direct(x, data=None, tile_scale_inv=None, skip=None):
     return library().fp8_block128_direct(x, data, tile_scale_inv, skip)
+
+
+def mxq_mxfp8_col_direct(x, layout="compact", data=None, scales=None):
+    return library().mxfp8_col_direct(x, layout, data, scales)
 
 
 def mxq_mxfp4_pack(x, layout="compact", packed=None, scales=None):

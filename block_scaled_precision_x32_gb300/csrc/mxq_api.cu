@@ -132,6 +132,24 @@ mxq_status mxq_mxfp4_pack(const void* x, mxq_dtype dt, int64_t rows, int64_t K, 
     return rowwise_quant(mxq::RowMode::MXFP4, x, dt, rows, K, ldx, packed, scales, lay, nullptr, stream);
 }
 
+mxq_status mxq_mxfp8_col_direct(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* data,
+                                uint8_t* scales, mxq_scale_layout lay, cudaStream_t stream) {
+    mxq_status st = check_dtype(dt);
+    if (st != MXQ_OK) return st;
+    if (!valid_shape(rows, K, ldx) || !valid_layout(lay)) return MXQ_ERR_INVALID_ARG;
+    if (rows == 0 || K == 0) return MXQ_OK;
+    if (!x || !data || !scales || !aligned(x, elt_size(dt))) return MXQ_ERR_INVALID_ARG;
+    mxq::ColwiseArgs a{};
+    a.x = x;
+    a.data = data;
+    a.scales = scales;
+    a.rows = rows;
+    a.K = K;
+    a.ldx = ldx;
+    a.lay = (int)lay;
+    return launch_status(mxq::launch_colwise(elt_of(dt), a, stream));
+}
+
 mxq_status mxq_fp8_block128_direct_update(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
                                           uint8_t* data, float* tile_scale_inv, const int32_t* skip,
                                           cudaStream_t stream) {
@@ -163,7 +181,8 @@ mxq_status mxq_dequantize(const mxq_quantized* q, void* out, mxq_dtype out_dt, c
     mxq_status st = check_dtype(out_dt);
     if (st != MXQ_OK) return st;
     if (!valid_shape(q->rows, q->K, q->K)) return MXQ_ERR_INVALID_ARG;
-    if (q->kind != MXQ_QUANT_MXFP8_ROW && q->kind != MXQ_QUANT_FP8_BLOCK128 && q->kind != MXQ_QUANT_MXFP4)
+    if (q->kind != MXQ_QUANT_MXFP8_ROW && q->kind != MXQ_QUANT_FP8_BLOCK128 && q->kind != MXQ_QUANT_MXFP4 &&
+        q->kind != MXQ_QUANT_MXFP8_COL)
         return MXQ_ERR_INVALID_ARG;
     if (q->kind != MXQ_QUANT_MXFP4 && q->fp8 != MXQ_E4M3 && q->fp8 != MXQ_E5M2) return MXQ_ERR_INVALID_ARG;
     if (q->kind == MXQ_QUANT_FP8_BLOCK128 && q->fp8 != MXQ_E4M3) return MXQ_ERR_INVALID_ARG;
@@ -184,6 +203,7 @@ mxq_status mxq_dequantize(const mxq_quantized* q, void* out, mxq_dtype out_dt, c
     a.tile_scale_inv = q->tile_scale_inv;
     a.out = out;
     a.out_bf16 = out_dt == MXQ_BF16;
+    if (q->kind == MXQ_QUANT_MXFP8_COL) return launch_status(mxq::launch_colwise_dequant(a, stream));
     return launch_status(mxq::launch_dequant(a, stream));
 }
 

@@ -1,0 +1,332 @@
+// mxq_colwise.cu -- direct MXFP4 -> MXFP8 columnwise (32x1 blocks) and its
+// dequantize.
+//
+// TE PR #3264 "MXFP4 weight QAT on MXFP8 and FP8 block-scaling recipes",
+// Description, mode 2: "MXFP8 columnwise = fresh 32x1 quantization with the
+// host amax rule" of the projected weight.  The host rule is read as the
+// round-up power of two: s = ceil(log2(amax / 448)) clamped to [-127, 127]
+// (zero amax: -127), payloads RTNE_E4M3(y / 2^s).
+//
+// One CTA per 32-row band x 256 columns: warp w owns the 32x32 tile of
+// columns 32w.., lane t its row.  The lane projects its 1x32 row block in
+// registers (the projection never goes back to HBM), stages it in a padded
+// shared tile, reads its column back for the 32x1 amax and exponent, and
+// then encodes its row with the 32 column scales -- one 32-byte payload
+// store per lane.  Only __syncwarp() between the steps.
+#include <cuda_runtime.h>
+
+#include "mxq_device.cuh"
+#include "mxq_internal.h"
+
+namespace mxq {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+
+__device__ __forceinline__ int64_t scale_offset(int64_t r, int64_t j, int64_t nb, int64_t Cp, int lay) {
+    if (lay == 0) return r * nb + j;
+    if (lay == 1) return r * Cp + j;
+    return ((r >> 7) * (Cp >> 2) + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+
+template <Elt ELT>
+struct CW;
+template <>
+struct CW<Elt::BF16> {
+    static constexpr int ES = 2, SEGS = 2, SEG_ELEMS = 16, MANT = 7, ROW_WORDS = 16 + 4;  // 64 B + 16 B pad
+};
+template <>
+struct CW<Elt::FP32> {
+    static constexpr int ES = 4, SEGS = 4, SEG_ELEMS = 8, MANT = 23, ROW_WORDS = 32 + 4;  // 128 B + 16 B pad
+};
+
+// Host MXFP8 exponent from the magnitude pattern of a finite amax:
+// amax = (1 + f) * 2^E, amax / 448 = ((1 + f) / 1.75) * 2^(E - 8), so
+// ceil(log2(amax / 448)) = E - 8 + [1 + f > 1.75].  Zero and subnormal
+// amax fall below 448 * 2^-127 and clamp to -127.
+template <int MANT>
+__device__ __forceinline__ int host_exponent(uint32_t amax_mag) {
+    const int E = (int)(amax_mag >> MANT);
+    const uint32_t frac = amax_mag & ((1u << MANT) - 1u);
+    int s = E - 135 + (frac > (3u << (MANT - 2)) ? 1 : 0);
+    s = E == 0 ? -127 : s;
+    return min(max(s, -127), 127);
+}
+
+template <Elt ELT, bool VEC, int DST>
+__global__ void __launch_bounds__(kThreads) colwise_kernel(ColwiseArgs a, int64_t bands) {
+    using P = CW<ELT>;
+    __shared__ __align__(16) uint32_t tile[kWarps][32 * P::ROW_WORDS];
+    __shared__ __align__(16) uint32_t colmul[kWarps][32];
+    const int w = threadIdx.x >> 5, t = threadIdx.x & 31;
+    const int64_t nb = (a.K + 31) >> 5;                  // 1x32 blocks per row
+    const int64_t nbr = (a.rows + 31) >> 5;              // 32x1 blocks per column
+    const int64_t Cpt = (nbr + 3) & ~int64_t(3);         // padded columns of the transposed scale matrix
+    const int64_t jb = (int64_t)blockIdx.x * kWarps + w;  // 1x32 block column of this warp
+    const int64_t col0 = jb * 32;
+    uint32_t* my = tile[w] + t * P::ROW_WORDS;
+
+    for (int64_t band = blockIdx.y; band < bands; band += gridDim.y) {
+        const int64_t r = band * 32 + t;
+        const int valid = (r < a.rows && jb < nb) ? (int)min((int64_t)32, a.K - col0) : 0;
+        uint32_t v[P::SEGS][8];
+        const char* xp = static_cast<const char*>(a.x) + (r * a.ldx + col0) * P::ES;
+#pragma unroll
+        for (int s = 0; s < P::SEGS; ++s) {
+            if constexpr (VEC) {
+                if (s * P::SEG_ELEMS < valid) {
+                    ld32(v[s], xp + 32 * s);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) v[s][k] = 0u;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    uint32_t word = 0u;
+                    if constexpr (ELT == Elt::BF16) {
+                        const int i0 = s * 16 + 2 * k;
+                        if (i0 < valid) word = reinterpret_cast<const uint16_t*>(xp)[i0];
+                        if (i0 + 1 < valid) word |= (uint32_t)reinterpret_cast<const uint16_t*>(xp)[i0 + 1] << 16;
+                    } else {
+                        const int i0 = s * 8 + k;
+                        if (i0 < valid) word = reinterpret_cast<const uint32_t*>(xp)[i0];
+                    }
+                    v[s][k] = word;
+                }
+            }
+        }
+
+        // projection of the lane's 1x32 row block (same rule and arithmetic as mxq_fake_quant_mxfp4)
+        uint32_t m = 0u;
+        if constexpr (ELT == Elt::BF16) {
+#pragma unroll
+            for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m = bf2_absmax(m, v[s][k]);
+            m &= 0x7FFF7FFFu;
+            m = max(m & 0xFFFFu, m >> 16);
+        } else {
+#pragma unroll
+            for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m = f32_absmax(m, v[s][k]);
+            m &= 0x7FFFFFFFu;
+        }
+        const bool poisoned = m >= (ELT == Elt::BF16 ? 0x7F80u : 0x7F800000u);
+        const int e = block_exponent<P::MANT>(m);
+        if constexpr (ELT == Elt::BF16) {
+            const Bf16Grid g = bf16_grid_unit(e);
+            const uint32_t scl = bf16_pow2_pair(e);
+#pragma unroll
+            for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    uint32_t y = bf2_grid(v[s][k], g);
+                    if (e == 125) y = bf2_sat(y, 0x40C040C0u);
+                    v[s][k] = poisoned ? 0x7FC07FC0u : (bf2_mul(y, scl) | (v[s][k] & 0x80008000u));
+                }
+        } else {
+            const uint32_t mult = f32_pow2(-e), scl = f32_pow2(e);
+#pragma unroll
+            for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    uint32_t y = f32_grid(v[s][k], mult);
+                    if (e == 125) y = f32_sat(y);
+                    v[s][k] = poisoned ? 0x7FC00000u : (f32_mul(y, scl) | (v[s][k] & 0x80000000u));
+                }
+        }
+        // rows and columns outside the tensor hold +0: they add nothing to a column amax
+        if (valid < 32) {
+#pragma unroll
+            for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int i0 = ELT == Elt::BF16 ? s * 16 + 2 * k : s * 8 + k;
+                    if (ELT == Elt::BF16) {
+                        if (i0 >= valid) v[s][k] &= 0xFFFF0000u;
+                        if (i0 + 1 >= valid) v[s][k] &= 0x0000FFFFu;
+                    } else if (i0 >= valid) {
+                        v[s][k] = 0u;
+                    }
+                }
+        }
+#pragma unroll
+        for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+                *reinterpret_cast<uint4*>(my + 8 * s + 4 * q) =
+                    make_uint4(v[s][4 * q], v[s][4 * q + 1], v[s][4 * q + 2], v[s][4 * q + 3]);
+        __syncwarp();
+
+        // column t of the warp's tile: 32x1 amax, host exponent, scale byte
+        uint32_t cm = 0u;
+        bool cpois = false;
+#pragma unroll 8
+        for (int rr = 0; rr < 32; ++rr) {
+            uint32_t mag;
+            if constexpr (ELT == Elt::BF16)
+                mag = (reinterpret_cast<const uint16_t*>(tile[w] + rr * P::ROW_WORDS)[t]) & 0x7FFFu;
+            else
+                mag = tile[w][rr * P::ROW_WORDS + t] & 0x7FFFFFFFu;
+            cpois |= mag >= (ELT == Elt::BF16 ? 0x7F80u : 0x7F800000u);
+            cm = max(cm, mag);
+        }
+        const int sx = host_exponent<P::MANT>(cm);
+        colmul[w][t] = cpois ? 0u : f32_pow2(-sx);  // 0 marks a poisoned column block
+        const int64_t c = col0 + t;
+        if (c < a.K && band < nbr) a.scales[scale_offset(c, band, nbr, Cpt, a.lay)] = (uint8_t)(cpois ? 255 : sx + 127);
+        __syncwarp();
+
+        // encode the lane's row with the column scales
+        uint32_t mul[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint4 mq = *reinterpret_cast<const uint4*>(&colmul[w][4 * q]);
+            mul[4 * q] = mq.x;
+            mul[4 * q + 1] = mq.y;
+            mul[4 * q + 2] = mq.z;
+            mul[4 * q + 3] = mq.w;
+        }
+        uint32_t b[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint32_t f[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = 4 * q + u;
+                uint32_t yv;
+                if constexpr (ELT == Elt::BF16) {
+                    const uint32_t word = v[i >> 4][(i & 15) >> 1];
+                    yv = (i & 1) ? (word & 0xFFFF0000u) : (word << 16);
+                } else {
+                    yv = v[i >> 3][i & 7];
+                }
+                f[u] = f32_mul(yv, mul[i]);
+            }
+            uint32_t bytes = e4m3x2_from_f32(f[1], f[0]) | (e4m3x2_from_f32(f[3], f[2]) << 16);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (mul[4 * q + u] == 0u) bytes = (bytes & ~(0xFFu << (8 * u))) | (0x7Fu << (8 * u));  // poisoned column block
+            b[q] = bytes;
+        }
+        if (valid > 0) {
+            uint8_t* d = a.data + r * a.K + col0;
+            if constexpr (DST == 2) {
+                st32(d, b);
+            } else if constexpr (DST == 1) {
+                st16(d, b[0], b[1], b[2], b[3]);
+                if (valid > 16) st16(d + 16, b[4], b[5], b[6], b[7]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if (k < valid) d[k] = (uint8_t)(b[k >> 2] >> ((k & 3) * 8));
+            }
+        }
+        __syncwarp();  // the tile is rewritten by the next band
+    }
+
+    if (a.lay != 0 && blockIdx.y == 0) {
+        // zero the padding of the padded / swizzled (transposed) scale buffer
+        const int64_t Rp = (a.K + 127) & ~int64_t(127);
+        const int64_t extra = Cpt - nbr;
+        const int64_t padA = a.K * extra, padB = (Rp - a.K) * Cpt;
+        for (int64_t p = (int64_t)blockIdx.x * kThreads + threadIdx.x; p < padA + padB; p += (int64_t)gridDim.x * kThreads) {
+            int64_t rr, jj;
+            if (p < padA) {
+                rr = p / extra;
+                jj = nbr + (p - rr * extra);
+            } else {
+                const int64_t q = p - padA;
+                rr = a.K + q / Cpt;
+                jj = q - (rr - a.K) * Cpt;
+            }
+            a.scales[scale_offset(rr, jj, nbr, Cpt, a.lay)] = 0;
+        }
+    }
+}
+
+// Dequantize of the columnwise form: out[r, c] = payload * 2^(code(c, r/32) - 127).
+// One thread per (32-row band, column), consecutive threads on consecutive
+// columns, so every row access of a warp is contiguous.
+template <bool E5M2, bool BF16OUT>
+__global__ void __launch_bounds__(kThreads) colwise_dequant_kernel(DequantArgs a) {
+    const int64_t nbr = (a.rows + 31) >> 5;
+    const int64_t Cpt = (nbr + 3) & ~int64_t(3);
+    const int64_t total = nbr * a.K;
+    for (int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * kThreads) {
+        const int64_t band = idx / a.K, c = idx - band * a.K;
+        const uint32_t code = a.scales[scale_offset(c, band, nbr, Cpt, a.lay)];
+        const uint32_t scale = code == 255u ? 0x7FC00000u : f32_pow2((int)code - 127);
+        const int64_t r1 = min(a.rows, band * 32 + 32);
+        for (int64_t r = band * 32; r < r1; ++r) {
+            const uint32_t b = a.data[r * a.K + c];
+            const uint32_t mag = b & 0x7Fu;
+            uint32_t f;
+            bool nan;
+            if constexpr (E5M2) {
+                f = f32_mul((mag << 21) | ((b & 0x80u) << 24), 0x77800000u);
+                nan = mag > 0x7Cu;
+                if (mag == 0x7Cu) f = 0x7F800000u | ((b & 0x80u) << 24);
+            } else {
+                f = f32_mul((mag << 20) | ((b & 0x80u) << 24), 0x7B800000u);
+                nan = mag == 0x7Fu;
+            }
+            uint32_t o = f32_mul(f, scale);
+            if (nan || (o & 0x7FFFFFFFu) > 0x7F800000u) o = 0x7FC00000u;
+            if constexpr (BF16OUT)
+                static_cast<uint16_t*>(a.out)[r * a.K + c] = (uint16_t)((o + 0x7FFFu + ((o >> 16) & 1u)) >> 16);
+            else
+                static_cast<uint32_t*>(a.out)[r * a.K + c] = o;
+        }
+    }
+}
+
+bool aligned(const void* p, int64_t n) { return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)n) == 0; }
+
+template <Elt ELT, bool VEC, int DST>
+cudaError_t launch_one(const ColwiseArgs& a, cudaStream_t s) {
+    const int64_t nb = ceil_div(a.K, 32), bands = ceil_div(a.rows, 32);
+    const int64_t gx = ceil_div(nb, kWarps);
+    const unsigned gy = (unsigned)(bands < 65535 ? bands : 65535);
+    colwise_kernel<ELT, VEC, DST><<<dim3((unsigned)gx, gy), kThreads, 0, s>>>(a, bands);
+    return cudaGetLastError();
+}
+
+template <Elt ELT>
+cudaError_t dispatch(const ColwiseArgs& a, cudaStream_t s) {
+    const int es = ELT == Elt::BF16 ? 2 : 4;
+    const bool vec = aligned(a.x, 32) && (a.ldx * es) % 32 == 0 && (a.K * es) % 32 == 0;
+    const int dst = (aligned(a.data, 32) && a.K % 32 == 0) ? 2 : (aligned(a.data, 16) && a.K % 16 == 0) ? 1 : 0;
+    if (!vec) return launch_one<ELT, false, 0>(a, s);
+    if (dst == 2) return launch_one<ELT, true, 2>(a, s);
+    if (dst == 1) return launch_one<ELT, true, 1>(a, s);
+    return launch_one<ELT, true, 0>(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_colwise(Elt elt, const ColwiseArgs& a, cudaStream_t s) {
+    return elt == Elt::BF16 ? dispatch<Elt::BF16>(a, s) : dispatch<Elt::FP32>(a, s);
+}
+
+cudaError_t launch_colwise_dequant(const DequantArgs& a, cudaStream_t s) {
+    const int64_t total = ceil_div(a.rows, 32) * a.K;
+    int64_t grid = ceil_div(total, (int64_t)kThreads);
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    const bool e5 = a.fp8 == 1;
+    if (e5)
+        a.out_bf16 ? colwise_dequant_kernel<true, true><<<(unsigned)grid, kThreads, 0, s>>>(a)
+                   : colwise_dequant_kernel<true, false><<<(unsigned)grid, kThreads, 0, s>>>(a);
+    else
+        a.out_bf16 ? colwise_dequant_kernel<false, true><<<(unsigned)grid, kThreads, 0, s>>>(a)
+                   : colwise_dequant_kernel<false, false><<<(unsigned)grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace mxq

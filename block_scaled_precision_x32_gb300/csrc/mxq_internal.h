@@ -29,8 +29,16 @@ struct Block128Args {
     const int32_t* skip;  // optional device flag: nonzero = write nothing
 };
 
+struct ColwiseArgs {
+    const void* x;
+    uint8_t* data;    // [rows, K] E4M3
+    uint8_t* scales;  // transposed scale matrix (K x ceil(rows/32)) in `lay`
+    int64_t rows, K, ldx;
+    int lay;
+};
+
 struct DequantArgs {
-    int kind;  // mxq_quant_kind (0 MXFP8 row, 1 128x128, 2 packed MXFP4)
+    int kind;  // mxq_quant_kind (0 MXFP8 row, 1 128x128, 2 packed MXFP4, 3 MXFP8 columnwise)
     const uint8_t* data;
     int64_t rows, K;
     int fp8;   // mxq_fp8
@@ -53,6 +61,8 @@ cudaError_t launch_rowwise(RowMode mode, Elt elt, const RowwiseArgs& a, cudaStre
 cudaError_t launch_block128(Elt elt, const Block128Args& a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
 cudaError_t launch_export(const ExportArgs& a, cudaStream_t s);
+cudaError_t launch_colwise(Elt elt, const ColwiseArgs& a, cudaStream_t s);
+cudaError_t launch_colwise_dequant(const DequantArgs& a, cudaStream_t s);
 
 // Resident-grid sizing: number of SMs of the current device (cached).
 int sm_count();

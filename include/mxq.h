@@ -158,6 +158,26 @@ MXQ_API mxq_status mxq_fp8_block128_direct(const void* x, mxq_dtype dt, int64_t 
 MXQ_API mxq_status mxq_mxfp4_pack(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* packed,
                                   uint8_t* scales, mxq_scale_layout lay, cudaStream_t stream);
 
+/* Direct MXFP4 -> MXFP8 columnwise (32x1 blocks) of the projected weight.
+ * Source: TE PR #3264, Description, mode 2: "MXFP8 columnwise = fresh 32x1
+ * quantization with the host amax rule" (its bytes match quantizing the
+ * mode-1 projection).  The pages do not state the host rule; it is read as
+ * the round-up power of two of MXFP8 quantizers: for each 32x1 block (rows
+ * 32i..32i+31 of column c, the last may be shorter) of y =
+ * mxq_fake_quant_mxfp4(x), s = ceil(log2(max|y| / 448)) clamped to
+ * [-127, 127] (a zero block gives -127), UE8M0 code s + 127, payloads
+ * RTNE_E4M3(y / 2^s), subnormals included (never saturating).  A block
+ * holding a NaN (from a poisoned 1x32 block) gets code 0xFF and payloads
+ * 0x7F.
+ *   x:      [rows, ldx] bf16 or fp32.
+ *   data:   [rows, K] E4M3 bytes, contiguous (quantized along rows).
+ *   scales: the column scales as the K x ceil(rows/32) matrix of the
+ *           transposed tensor -- scale (c, i) at c*ceil(rows/32) + i when
+ *           COMPACT -- in layout `lay`: mxq_scale_bytes(K, rows, lay) bytes.
+ * Errors: as mxq_mxfp8_row_direct. */
+MXQ_API mxq_status mxq_mxfp8_col_direct(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                        uint8_t* data, uint8_t* scales, mxq_scale_layout lay, cudaStream_t stream);
+
 /* Skip-update variants of the converters, for cached weights updated inside
  * a captured CUDA graph (TE PR #3264, review: a direct cache-hit update must
  * honour the skip-update flag of CUDA-graph replays).  `skip` is a device
@@ -173,7 +193,12 @@ MXQ_API mxq_status mxq_fp8_block128_direct_update(const void* x, mxq_dtype dt, i
                                                   uint8_t* data, float* tile_scale_inv, const int32_t* skip,
                                                   cudaStream_t stream);
 
-typedef enum { MXQ_QUANT_MXFP8_ROW = 0, MXQ_QUANT_FP8_BLOCK128 = 1, MXQ_QUANT_MXFP4 = 2 } mxq_quant_kind;
+typedef enum {
+    MXQ_QUANT_MXFP8_ROW = 0,
+    MXQ_QUANT_FP8_BLOCK128 = 1,
+    MXQ_QUANT_MXFP4 = 2,
+    MXQ_QUANT_MXFP8_COL = 3 /* scales: the transposed K x ceil(rows/32) matrix in `lay` */
+} mxq_quant_kind;
 
 /* A quantized tensor of rows x K as read by mxq_dequantize. */
 typedef struct {
@@ -190,7 +215,8 @@ typedef struct {
  * (the export decodes to dequantize() exactly); TE PR #3264, Description
  * (UE8M0 decode: code 0 is 2^-127, code 255 is NaN).
  * MXFP8_ROW: out = payload * 2^(code - 127); BLOCK128: out = payload *
- * tile_scale_inv; MXFP4: out = E2M1 value * 2^(code - 127).  fp32 output is
+ * tile_scale_inv; MXFP4: out = E2M1 value * 2^(code - 127); MXFP8_COL: out =
+ * payload * 2^(code(c, r/32) - 127).  fp32 output is
  * that product rounded to nearest even (exact for power-of-two scales, Inf
  * on overflow, e.g. 4 * 2^126); bf16 output is one more
  * round-to-nearest-even of the fp32 value.

@@ -75,6 +75,9 @@ def _L():
             lib.oracle_e8m0_value.argtypes = [ctypes.c_uint8]
             lib.oracle_e8m0_value.restype = ctypes.c_double
             lib.oracle_mxfp4_pack.argtypes = [vp, ip, i64, i64, i64, vp, vp]
+            lib.oracle_mxfp8_col_direct.argtypes = [vp, ip, i64, i64, i64, vp, vp]
+            lib.oracle_mxfp8_host_exponent.argtypes = [ctypes.c_double]
+            lib.oracle_mxfp8_host_exponent.restype = ip
             lib.oracle_dequant_mxfp4.argtypes = [vp, vp, ip, i64, i64, vp, ip]
             lib.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
             lib.oracle_e2m1_value.restype = ctypes.c_double
@@ -200,6 +203,25 @@ def mxfp4_pack(x: np.ndarray, lay: int = COMPACT):
     if lay == COMPACT:
         return packed, compact
     return packed, scales_to_layout(compact, rows, K, lay)
+
+
+def mxfp8_col_direct(x: np.ndarray, lay: int = COMPACT):
+    """Direct MXFP8 columnwise: (E4M3 bytes [rows, K], scales of the K x
+    ceil(rows/32) transposed scale matrix in ``lay``)."""
+    dt = _dt_of(x)
+    rows, K, ldx = _rows_k_ld(x)
+    data = np.empty((rows, K), dtype=np.uint8)
+    nbr = (rows + 31) // 32
+    compact = np.empty((K, nbr), dtype=np.uint8)
+    if x.size:
+        _L().oracle_mxfp8_col_direct(_ptr(x), dt, rows, K, ldx, _ptr(data), _ptr(compact))
+    if lay == COMPACT:
+        return data, compact
+    return data, scales_to_layout(compact, K, rows, lay)
+
+
+def mxfp8_host_exponent(amax: float) -> int:
+    return int(_L().oracle_mxfp8_host_exponent(amax))
 
 
 def dequant_mxfp4(packed: np.ndarray, scales: np.ndarray, lay: int, K: int, out_dt: int) -> np.ndarray:

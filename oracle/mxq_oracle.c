@@ -489,6 +489,68 @@ int oracle_dequant_block128(const uint8_t* data, const float* tile_scale_inv, in
     return OR_OK;
 }
 
+/* -------------------------------------------------- MXFP8 columnwise */
+
+/* Scale exponent of the host MXFP8 quantizer for a 32x1 block: the smallest
+ * s with amax <= 448 * 2^s (448 = E4M3's largest finite), i.e.
+ * ceil(log2(amax / 448)), clamped to [-127, 127]; a zero amax gives -127.
+ * Reading: the pages name "the host amax rule" without stating it; this is
+ * the round-up power-of-two rule of MXFP8 quantizers, under which
+ * amax / 2^s never exceeds 448. */
+int oracle_mxfp8_host_exponent(double amax) {
+    if (amax == 0.0) return -127;
+    int s = ilogb(amax) - 12;
+    while (ldexp(448.0, s) < amax) ++s;
+    while (ldexp(448.0, s - 1) >= amax) --s;
+    if (s < -127) s = -127;
+    if (s > 127) s = 127;
+    return s;
+}
+
+/* Direct MXFP8 columnwise (TE PR #3264, Description, mode 2: "MXFP8
+ * columnwise = fresh 32x1 quantization with the host amax rule"; its bytes
+ * match quantizing the projected weight): y = projection of x, then for
+ * each 32x1 block (rows 32i..32i+31 of column c; the last may be shorter)
+ * the host exponent s of max|y|, UE8M0 code s + 127 and payloads
+ * RTNE_E4M3(y / 2^s).  A block holding a NaN (from a poisoned 1x32 block)
+ * gets code 0xFF and payloads 0x7F.  data is [rows, K]; scales are compact
+ * and transposed: scale (c, i) at c * ceil(rows/32) + i. */
+int oracle_mxfp8_col_direct(const void* x, int dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* data,
+                            uint8_t* scales) {
+    if (dt != OR_BF16 && dt != OR_FP32) return OR_BAD;
+    size_t es = dt == OR_BF16 ? 2 : 4;
+    int64_t nbr = (rows + 31) / 32;
+    void* y = malloc((size_t)(rows * K) * es + 1);
+    if (!y) abort();
+    oracle_fake_quant_mxfp4(x, y, dt, rows, K, ldx, K);
+    for (int64_t c = 0; c < K; ++c) {
+        for (int64_t i = 0; i < nbr; ++i) {
+            int64_t r0 = 32 * i, r1 = r0 + 32 < rows ? r0 + 32 : rows;
+            int poisoned = 0;
+            double amax = 0.0;
+            for (int64_t r = r0; r < r1; ++r) {
+                uint32_t bits = load_bits(y, dt, r * K + c);
+                if (is_nonfinite(bits, dt)) poisoned = 1;
+                else if (abs_value(bits, dt) > amax) amax = abs_value(bits, dt);
+            }
+            if (poisoned) {
+                scales[c * nbr + i] = 0xFF;
+                for (int64_t r = r0; r < r1; ++r) data[r * K + c] = 0x7F;
+                continue;
+            }
+            int sx = oracle_mxfp8_host_exponent(amax);
+            scales[c * nbr + i] = (uint8_t)(sx + 127);
+            for (int64_t r = r0; r < r1; ++r) {
+                uint32_t bits = load_bits(y, dt, r * K + c);
+                double v = ldexp(abs_value(bits, dt), -sx);
+                data[r * K + c] = oracle_e4m3_rtne(sign_of(bits, dt) ? -v : v);
+            }
+        }
+    }
+    free(y);
+    return OR_OK;
+}
+
 /* ------------------------------------------------------ packed MXFP4 */
 
 /* Packed MXFP4 deployment form (TE PR #3264, Description: training sees

@@ -75,6 +75,25 @@ def run_all_and_compare(mx, x_np, layouts=LAYOUTS, block128=True, guard=True):
                 np.testing.assert_array_equal(host_bits(a), want)
                 np.testing.assert_array_equal(host_bits(b), want)  # export decodes to dequantize()
 
+    # MXFP8 columnwise (32x1 blocks of the projection), each layout, and its dequantize
+    ref_cd, ref_cs = oracle.mxfp8_col_direct(x_np, oracle.COMPACT)
+    x2 = x if x.dim() == 2 else x.reshape(rows, K)
+    for lay in layouts:
+        nbytes = mx.scale_bytes(K, rows, lay)
+        d = Guarded((rows, K), torch.uint8)
+        s = Guarded((max(nbytes, 1),), torch.uint8)
+        mx.mxfp8_col_direct(x2, lay, data=d.t, scales=s.t)
+        torch.cuda.synchronize()
+        assert d.intact() and s.intact()
+        np.testing.assert_array_equal(host_bits(d.t), ref_cd)
+        ref_lay = ref_cs.reshape(-1) if lay == oracle.COMPACT else oracle.scales_to_layout(ref_cs, K, rows, lay)
+        np.testing.assert_array_equal(host_bits(s.t)[:nbytes], ref_lay)
+        for odt, ocode in ((torch.float32, oracle.FP32), (torch.bfloat16, oracle.BF16)):
+            got = mx.dequantize(d.t, scales=s.t[:nbytes], layout=lay, out_dtype=odt, columnwise=True)
+            torch.cuda.synchronize()
+            want = oracle.dequant_mxfp8(np.ascontiguousarray(ref_cd.T), ref_cs, oracle.COMPACT, oracle.E4M3, ocode).T
+            np.testing.assert_array_equal(host_bits(got), oracle_bits(np.ascontiguousarray(want)))
+
     # packed MXFP4 (deployment form), each scale layout, and its dequantize
     ref_p, ref_pc = oracle.mxfp4_pack(x_np, oracle.COMPACT)
     for lay in layouts:
@@ -309,6 +328,31 @@ def test_large_bf16_8192_sampled(mx):
         rd, rs = oracle.fp8_block128_direct(x_np[sl])
         np.testing.assert_array_equal(host_bits(bd[sl]), rd)
         np.testing.assert_array_equal(host_bits(bs[band]), rs.view(np.uint32)[0])
+
+
+def test_large_bf16_columnwise_and_packed_sampled(mx):
+    """8192 x 8192 bf16: MXFP8 columnwise (swizzled transposed scales) and
+    packed MXFP4 at full size; sampled 32-row bands against the oracle, and
+    over the whole tensor the packed form decodes to the projection."""
+    x_np = syn.normal_bf16(8192, 8192)
+    x = dev_bf16(x_np)
+    cd, cs = mx.mxfp8_col_direct(x, "compact")
+    cd2, cs2 = mx.mxfp8_col_direct(x, "swizzled")
+    p, ps = mx.mxfp4_pack(x, "swizzled")
+    y = mx.fake_quant_mxfp4(x)
+    back = mx.dequantize(p, scales=ps, layout="swizzled", out_dtype=torch.bfloat16, mxfp4_K=8192)
+    torch.cuda.synchronize()
+    assert torch.equal(back.view(torch.int16), y.view(torch.int16))
+    assert torch.equal(cd, cd2)
+    comp = mx.export_mxfp8(torch.empty((8192, 8192), dtype=torch.uint8, device="cuda"), cs2, shape=(8192, 8192),
+                           layout="swizzled")
+    torch.cuda.synchronize()
+    assert torch.equal(comp.scale_inv, cs)
+    for band in (0, 101, 255):
+        sl = slice(band * 32, band * 32 + 32)
+        rd, rs = oracle.mxfp8_col_direct(x_np[sl])
+        np.testing.assert_array_equal(host_bits(cd[sl]), rd)
+        np.testing.assert_array_equal(host_bits(cs[:, band]), rs[:, 0])
 
 
 def _tile_spread(x_np):

@@ -23,6 +23,10 @@ MUTANTS = {
     "scale rule: dropped -1": ("return (E - f.bias) - 2 + (m > half ? 1 : 0);", "return (E - f.bias) - 1 + (m > half ? 1 : 0);"),
     "scale rule: lower clamp -127": ("    if (e < -126) e = -126;\n    if (e > 125) e = 125;", "    if (e < -127) e = -127;\n    if (e > 125) e = 125;"),
     "scale rule: upper clamp 126": ("    if (e > 125) e = 125;\n", "    if (e > 125) e = 126;\n"),
+    "host rule: 224 instead of 448": ("while (ldexp(448.0, s) < amax) ++s;\n    while (ldexp(448.0, s - 1) >= amax) --s;",
+                                      "while (ldexp(224.0, s) < amax) ++s;\n    while (ldexp(224.0, s - 1) >= amax) --s;"),
+    "host rule: floor instead of ceil": ("    while (ldexp(448.0, s - 1) >= amax) --s;", "    while (ldexp(448.0, s - 1) >= amax) --s;\n    if (ldexp(448.0, s) > amax) --s;"),
+    "columnwise block of 16 rows": ("int64_t r0 = 32 * i, r1 = r0 + 32 < rows ? r0 + 32 : rows;", "int64_t r0 = 32 * i, r1 = r0 + 16 < rows ? r0 + 16 : rows;"),
     "packed MXFP4: upper clamp 125": ("            if (e > 126) e = 126;\n", "            if (e > 125) e = 125;\n"),
     "packed MXFP4: high nibble first": ("(uint8_t)(c << ((i % 2) * 4))", "(uint8_t)(c << ((1 - i % 2) * 4))"),
     "E2M1 ties to odd": ("if (dc < db || (dc == db && (c % 2) == 0)) best = c;\n    }\n    return best;\n}\n\ntypedef",

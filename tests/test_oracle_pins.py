@@ -348,6 +348,64 @@ def test_blockwise_poisoned_block_left_out_of_tile_max():
     np.testing.assert_array_equal(back.view(np.uint32)[finite], y.view(np.uint32)[finite])
 
 
+# ------------------------------------------------ MXFP8 columnwise (32x1)
+
+def test_mxfp8_host_exponent_is_ceil_log2_amax_over_448():
+    """The host rule read for "fresh 32x1 quantization": the smallest s with
+    amax <= 448 * 2^s, clamped to [-127, 127]; zero gives -127."""
+    from fractions import Fraction
+    g = np.random.default_rng(12)
+    vals = [p * 2.0 ** k for p in (0.5, 1, 1.5, 2, 3, 4, 6) for k in range(-133, 126)]
+    vals += [float(v) for v in g.uniform(0, 1, 3000).astype(np.float32) * np.ldexp(1.0, g.integers(-140, 120, 3000))]
+    vals += [448.0, 448.0 * 2 ** -20, 449.0, 447.9999, 2.0 ** -149, 3.0e38]
+    for v in vals:
+        if v == 0:
+            continue
+        a = Fraction(v)
+        s_ = 0
+        while Fraction(448) * Fraction(2) ** s_ < a:
+            s_ += 1
+        while Fraction(448) * Fraction(2) ** (s_ - 1) >= a:
+            s_ -= 1
+        assert oracle.mxfp8_host_exponent(v) == max(-127, min(127, s_)), v
+    assert oracle.mxfp8_host_exponent(0.0) == -127
+
+
+def test_mxfp8_columnwise_exact_for_uniform_row_exponents():
+    """When every 1x32 block of a column block shares one exponent, the
+    projected values p*2^e re-encode exactly (payload p*2^6 or p*2^7, s =
+    e - 6 or e - 7): decode(columnwise(x)) == projection(x)."""
+    g = np.random.default_rng(4)
+    grid = np.array([0.5, 1, 1.5, 2, 3, 4, 6, -0.5, -1, -1.5, -2, -3, -4, -6, 0], dtype=np.float64)
+    for e in (-126, -100, -3, 0, 17, 118):
+        p = grid[g.integers(0, 15, size=(96, 64))]
+        p[:, ::32] = 6.0  # every 1x32 block reaches 6, so its exponent is exactly e
+        x = (p * 2.0 ** e).astype(np.float32)
+        y = oracle.fake_quant_mxfp4(x)
+        data, sc = oracle.mxfp8_col_direct(x)
+        assert sc.shape == (64, 3)
+        back = oracle.dequant_mxfp8(np.ascontiguousarray(data.T), sc, oracle.COMPACT, oracle.E4M3, FP32).T
+        np.testing.assert_array_equal(np.ascontiguousarray(back).view(np.uint32), y.view(np.uint32))
+
+
+def test_mxfp8_columnwise_error_bound_and_poison():
+    """Mixed row exponents: every decoded value is the E4M3 rounding of y /
+    2^s (relative error <= 2^-4, absolute <= 2^(s-10) in the subnormal range);
+    a NaN in a 1x32 block poisons each 32x1 block it touches."""
+    x = syn.partial_block_fp32((100, 48))
+    y = oracle.fake_quant_mxfp4(x).astype(np.float64)
+    data, sc = oracle.mxfp8_col_direct(x)
+    assert sc.shape == (48, 4) and data.shape == (100, 48)
+    back = oracle.dequant_mxfp8(np.ascontiguousarray(data.T), sc, oracle.COMPACT, oracle.E4M3, FP32).T.astype(np.float64)
+    s_of = np.ldexp(1.0, sc.astype(np.int64).T - 127)  # (4, 48)
+    bound = np.maximum(np.abs(y) * 2.0 ** -4, np.repeat(s_of, 32, axis=0)[:100] * 2.0 ** -10)
+    assert np.all(np.abs(back - y) <= bound)
+    x[40, 5] = np.nan  # poisons row 40's first 1x32 block (columns 0..31)
+    data, sc = oracle.mxfp8_col_direct(x)
+    assert np.all(sc[:32, 1] == 0xFF) and np.all(sc[32:, 1] != 0xFF)
+    assert np.all(data[32:64, :32] == 0x7F)
+
+
 # ------------------------------------------------------ packed MXFP4
 
 def test_packed_mxfp4_decodes_to_projection_and_moves_past_the_cap():
