@@ -161,22 +161,32 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(ColwiseArgs a, int64_
                     make_uint4(v[s][4 * q], v[s][4 * q + 1], v[s][4 * q + 2], v[s][4 * q + 3]);
         __syncwarp();
 
-        // column t of the warp's tile: 32x1 amax, host exponent, scale byte
-        uint32_t cm = 0u;
-        bool cpois = false;
+        // 32x1 column maxima.  bf16: lane t scans the column pair (2p, 2p+1),
+        // p = t % 16, over rows 16h..16h+15, h = t / 16, with the packed
+        // NaN-propagating abs-max, joins the other half by one shuffle, and
+        // takes column 2p + h.  fp32: lane t scans column t.
+        uint32_t cm;
+        int cl;  // column of the tile this lane finishes
+        if constexpr (ELT == Elt::BF16) {
+            const int pr = t & 15, h = t >> 4;
+            uint32_t m2 = 0u;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) m2 = bf2_absmax(m2, tile[w][(16 * h + rr) * P::ROW_WORDS + pr]);
+            m2 = bf2_absmax(m2, __shfl_xor_sync(0xffffffffu, m2, 16));
+            cm = (h ? (m2 >> 16) : m2) & 0x7FFFu;
+            cl = 2 * pr + h;
+        } else {
+            uint32_t m1 = 0u;
 #pragma unroll 8
-        for (int rr = 0; rr < 32; ++rr) {
-            uint32_t mag;
-            if constexpr (ELT == Elt::BF16)
-                mag = (reinterpret_cast<const uint16_t*>(tile[w] + rr * P::ROW_WORDS)[t]) & 0x7FFFu;
-            else
-                mag = tile[w][rr * P::ROW_WORDS + t] & 0x7FFFFFFFu;
-            cpois |= mag >= (ELT == Elt::BF16 ? 0x7F80u : 0x7F800000u);
-            cm = max(cm, mag);
+            for (int rr = 0; rr < 32; ++rr) m1 = f32_absmax(m1, tile[w][rr * P::ROW_WORDS + t]);
+            cm = m1 & 0x7FFFFFFFu;
+            cl = t;
         }
+        const bool cpois = cm >= (ELT == Elt::BF16 ? 0x7F80u : 0x7F800000u);
         const int sx = host_exponent<P::MANT>(cm);
-        colmul[w][t] = cpois ? 0u : f32_pow2(-sx);  // 0 marks a poisoned column block
-        const int64_t c = col0 + t;
+        // a poisoned column block multiplies by NaN, which the E4M3 conversion turns into 0x7F
+        colmul[w][cl] = cpois ? 0x7FC00000u : f32_pow2(-sx);
+        const int64_t c = col0 + cl;
         if (c < a.K && band < nbr) a.scales[scale_offset(c, band, nbr, Cpt, a.lay)] = (uint8_t)(cpois ? 255 : sx + 127);
         __syncwarp();
 
@@ -206,11 +216,7 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(ColwiseArgs a, int64_
                 }
                 f[u] = f32_mul(yv, mul[i]);
             }
-            uint32_t bytes = e4m3x2_from_f32(f[1], f[0]) | (e4m3x2_from_f32(f[3], f[2]) << 16);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (mul[4 * q + u] == 0u) bytes = (bytes & ~(0xFFu << (8 * u))) | (0x7Fu << (8 * u));  // poisoned column block
-            b[q] = bytes;
+            b[q] = e4m3x2_from_f32(f[1], f[0]) | (e4m3x2_from_f32(f[3], f[2]) << 16);
         }
         if (valid > 0) {
             uint8_t* d = a.data + r * a.K + col0;

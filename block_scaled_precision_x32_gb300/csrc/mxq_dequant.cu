@@ -20,8 +20,10 @@
 // code for fp32 output take the element-wise fp32 path, which also makes
 // NaN canonical.  The 128x128 form multiplies by an arbitrary fp32
 // scale_inv and always takes the fp32 path.  Packed MXFP4 (16 bytes of
-// nibbles per block) decodes each E2M1 value exactly in fp32 and scales it
-// by 2^(code-127) (exact, or Inf past fp32's range).
+// nibbles per block) maps each E2M1 code to its bf16 pattern and scales it
+// by 2^(code-127) with one exact bf16 multiply (Inf past the range; the
+// value is exact in bf16 otherwise, 2^-128 included, so fp32 output is the
+// widened bf16).
 #include <cuda_runtime.h>
 
 #include "mxq_device.cuh"
@@ -134,13 +136,6 @@ __device__ __forceinline__ void store_out(void* out, const uint32_t* o, int vali
     }
 }
 
-// Signed E2M1 nibble -> fp32 pattern of its value.
-__device__ __forceinline__ uint32_t e2m1_f32(uint32_t nib) {
-    const uint32_t m = nib & 7u;
-    const uint32_t mag = m >= 2u ? 0x3F000000u + (m << 22) : (m ? 0x3F000000u : 0u);  // 1, 1.5, 2, 3, 4, 6 / 0.5 / 0
-    return mag | ((nib & 8u) << 28);
-}
-
 template <int SRC>
 __device__ __forceinline__ void load_nibbles(uint32_t (&w)[4], const uint8_t* p, int valid) {
     const int nbytes = (valid + 1) >> 1;
@@ -186,19 +181,31 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a, int64_
             uint32_t w[4];
             load_nibbles<SRC>(w, a.data + r * ((a.K + 1) >> 1) + j * 16, valid);
             const uint32_t c = a.scales[scale_offset(r, j, nb, Cp, a.lay)];
-            const uint32_t scale32 = c == 255u ? 0x7FC00000u : f32_pow2((int)c - 127);
+            // E2M1 magnitudes -> bf16 patterns by a byte table (high and low byte
+            // of 0, .5, 1, 1.5, 2, 3, 4, 6) indexed by PRMT, signs spread by one
+            // multiply, then one exact bf16 multiply by 2^(code-127) (Inf past
+            // bf16's range, as rounding the exact fp32 product would give).
+            const uint32_t scale16 = c == 0u ? 0x00400040u : ((c << 7) | (c << 23));
             uint32_t o[WORDS];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                uint32_t f = f32_mul(e2m1_f32((w[i >> 3] >> ((i & 7) * 4)) & 15u), scale32);
-                if ((f & 0x7FFFFFFFu) > 0x7F800000u) f = 0x7FC00000u;
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t nib = (w[q >> 1] >> ((q & 1) * 16)) & 0xFFFFu;  // elements 4q..4q+3
+                const uint32_t sel = nib & 0x7777u, sg = nib & 0x8888u;
+                const uint32_t hi4 = prmt(0x3F3F3F00u, 0x40404040u, sel);
+                const uint32_t lo4 = prmt(0xC0800000u, 0xC0804000u, sel);
+                uint32_t y0 = prmt(lo4, hi4, 0x5140u) | ((sg * 0x01001000u) & 0x80008000u);
+                uint32_t y1 = prmt(lo4, hi4, 0x7362u) | ((sg * 0x00010010u) & 0x80008000u);
+                y0 = bf2_mul(y0, scale16);
+                y1 = bf2_mul(y1, scale16);
+                if (c == 255u) y0 = y1 = 0x7FC07FC0u;
                 if constexpr (BF16OUT) {
-                    if (i & 1)
-                        o[i >> 1] |= bf16_rne(f) << 16;
-                    else
-                        o[i >> 1] = bf16_rne(f);
+                    o[2 * q] = y0;
+                    o[2 * q + 1] = y1;
                 } else {
-                    o[i] = f;
+                    o[4 * q] = y0 << 16;
+                    o[4 * q + 1] = y0 & 0xFFFF0000u;
+                    o[4 * q + 2] = y1 << 16;
+                    o[4 * q + 3] = y1 & 0xFFFF0000u;
                 }
             }
             store_out<BF16OUT, VOUT>(static_cast<char*>(a.out) + (r * a.K + col0) * (BF16OUT ? 2 : 4), o, valid);
