@@ -14,6 +14,8 @@ Functions carry the C names:
 * ``mxq_mxfp8_col_direct``     direct MXFP8 columnwise, 32x1 blocks (TE PR #3264, mode 2)
 * ``mxq_dequantize``           MXFP8 rowwise / 128x128 blockwise / packed MXFP4 -> bf16 / fp32
 * ``mxq_export_mxfp8``         export_components (TE PR #3790)
+* ``mxq_export_mxfp8_grouped`` export of many storages (per expert) in one launch
+* ``mxq_quantize_export_mxfp8`` quantize a bf16/fp32 weight and export it in one call
 
 The ``skip=`` argument of the converters selects the ``*_update`` entry
 points: a device int32 tensor, read when the kernel runs; nonzero means the
@@ -35,7 +37,7 @@ __all__ = [
     "MXQError", "MXFP8Components", "Library", "Call", "library",
     "mxq_fake_quant_mxfp4", "mxq_mxfp8_row_direct", "mxq_fp8_block128_direct",
     "mxq_dequantize", "mxq_export_mxfp8", "mxq_mxfp4_pack", "mxq_mxfp8_col_direct", "mxq_scale_bytes",
-    "mxq_tile_scale_count",
+    "mxq_tile_scale_count", "mxq_export_mxfp8_grouped", "mxq_quantize_export_mxfp8",
     "COMPACT", "PADDED", "SWIZZLED", "scale_cols",
 ]
 
@@ -160,6 +162,9 @@ class Library:
         L.mxq_fp8_block128_direct_update.argtypes = [vp, ci, i64, i64, i64, vp, vp, vp, vp]
         L.mxq_mxfp4_pack.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp]
         L.mxq_mxfp8_col_direct.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp]
+        L.mxq_export_mxfp8_grouped.argtypes = [ctypes.POINTER(_Storage), i64, vp, ctypes.c_size_t,
+                                               ctypes.POINTER(_Components), vp]
+        L.mxq_quantize_export_mxfp8.argtypes = [vp, ci, i64, i64, i64, vp, vp, ctypes.POINTER(_Components), vp]
         L.mxq_dequantize.argtypes = [ctypes.POINTER(_Quantized), vp, ci, vp]
         L.mxq_export_mxfp8.argtypes = [ctypes.POINTER(_Storage), vp, ctypes.c_size_t, ctypes.POINTER(_Components), vp]
         L.mxq_scale_bytes.argtypes = [i64, i64, ci]
@@ -170,7 +175,8 @@ class Library:
         L.mxq_status_string.restype = ctypes.c_char_p
         for fn in ("mxq_fake_quant_mxfp4", "mxq_mxfp8_row_direct", "mxq_fp8_block128_direct", "mxq_dequantize",
                    "mxq_export_mxfp8", "mxq_fake_quant_mxfp4_update", "mxq_mxfp8_row_direct_update",
-                   "mxq_fp8_block128_direct_update", "mxq_mxfp4_pack", "mxq_mxfp8_col_direct"):
+                   "mxq_fp8_block128_direct_update", "mxq_mxfp4_pack", "mxq_mxfp8_col_direct",
+                   "mxq_export_mxfp8_grouped", "mxq_quantize_export_mxfp8"):
             getattr(L, fn).restype = ci
         self.L = L
 
@@ -420,6 +426,79 @@ class Library:
         call()
         return comp
 
+    def export_mxfp8_grouped(self, storages, scale_out: Optional[torch.Tensor] = None):
+        """Export many MXFP8 storages at once.  ``storages`` is a list of
+        dicts with keys data, scales, shape, layout (default compact) and fp8
+        (default e4m3).  The copies share ``scale_out`` (allocated when None)
+        and run in one launch per 128 storages.  Returns MXFP8Components."""
+        n = len(storages)
+        st = (_Storage * max(n, 1))()
+        sizes, keep = [], []
+        dev = None
+        for g, d in enumerate(storages):
+            shape = tuple(d["shape"])
+            K = shape[-1] if shape else 0
+            rows = 1
+            for v in shape[:-1]:
+                rows *= v
+            data, scales = d.get("data"), d["scales"]
+            _need_cuda(data, scales)
+            dev = scales.device
+            st[g].data = data.data_ptr() if data is not None else None
+            st[g].scales = scales.data_ptr()
+            st[g].fp8 = _fp8_code(d.get("fp8", "e4m3"))
+            st[g].lay = _LAYOUTS[d.get("layout", "compact")]
+            st[g].rows, st[g].K = rows, K
+            nb = scale_cols(K)
+            view = st[g].lay == COMPACT or (st[g].lay == PADDED and nb % 4 == 0) or rows * K == 0
+            sizes.append((shape, rows, nb, view))
+            keep.append((data, scales))
+        need = sum(rows * nb for _, rows, nb, view in sizes if not view)
+        if scale_out is None and need:
+            scale_out = torch.empty(need, dtype=torch.uint8, device=dev)
+        comps = (_Components * max(n, 1))()
+        if n:
+            with torch.cuda.device(dev):
+                self._check(self.L.mxq_export_mxfp8_grouped(
+                    st, n, ctypes.c_void_p(scale_out.data_ptr()) if scale_out is not None else None,
+                    scale_out.numel() if scale_out is not None else 0, comps, _stream(keep[0][1])),
+                    "mxq_export_mxfp8_grouped")
+        out, off = [], 0
+        for g, (shape, rows, nb, view) in enumerate(sizes):
+            data, scales = keep[g]
+            fp8_dtype = torch.float8_e4m3fn if st[g].fp8 == _E4M3 else torch.float8_e5m2
+            values = data.view(fp8_dtype).view(shape) if data is not None else None
+            if view:
+                sc = scales.reshape(-1)[: rows * nb].view(shape[:-1] + (nb,))
+            else:
+                sc = scale_out[off: off + rows * nb].view(shape[:-1] + (nb,))
+                off += rows * nb
+            out.append(MXFP8Components(values, sc, bool(comps[g].is_view)))
+        return out
+
+    def quantize_export_mxfp8(self, x: torch.Tensor, data: Optional[torch.Tensor] = None,
+                              scales: Optional[torch.Tensor] = None) -> MXFP8Components:
+        """Quantize x (bf16/fp32) to MXFP8 rowwise (direct lift) and return the
+        exported values and compact scales in one call."""
+        _need_cuda(x, data, scales)
+        dt = _dt_code(x)
+        rows, K, ldx = _rows_view(x)
+        nb = scale_cols(K)
+        if data is None:
+            data = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        if scales is None:
+            scales = torch.empty(tuple(x.shape[:-1]) + (nb,), dtype=torch.uint8, device=x.device)
+        if not data.is_contiguous() or data.numel() != rows * K or not scales.is_contiguous() or scales.numel() < rows * nb:
+            raise ValueError("data must be rows*K contiguous bytes and scales rows*ceil(K/32)")
+        comp = _Components()
+        with torch.cuda.device(x.device):
+            self._check(self.L.mxq_quantize_export_mxfp8(ctypes.c_void_p(x.data_ptr()), dt, rows, K, ldx,
+                                                         ctypes.c_void_p(data.data_ptr()),
+                                                         ctypes.c_void_p(scales.data_ptr()), ctypes.byref(comp),
+                                                         _stream(x)), "mxq_quantize_export_mxfp8")
+        return MXFP8Components(data.view(torch.float8_e4m3fn).view(x.shape),
+                               scales.reshape(-1)[: rows * nb].view(tuple(x.shape[:-1]) + (nb,)), True)
+
 
 class Call:
     """A prepared libmxq call (see Library.plan_*)."""
@@ -478,6 +557,14 @@ def mxq_dequantize(data, **kw):
 
 def mxq_export_mxfp8(data, scales, **kw):
     return library().export_mxfp8(data, scales, **kw)
+
+
+def mxq_export_mxfp8_grouped(storages, scale_out=None):
+    return library().export_mxfp8_grouped(storages, scale_out)
+
+
+def mxq_quantize_export_mxfp8(x, data=None, scales=None):
+    return library().quantize_export_mxfp8(x, data, scales)
 
 
 def mxq_scale_bytes(rows, K, layout="compact"):

@@ -207,29 +207,43 @@ mxq_status mxq_dequantize(const mxq_quantized* q, void* out, mxq_dtype out_dt, c
     return launch_status(mxq::launch_dequant(a, stream));
 }
 
-mxq_status mxq_export_mxfp8(const mxq_mxfp8_storage* st, uint8_t* scale_out, size_t scale_out_bytes,
-                            mxq_mxfp8_components* out, cudaStream_t stream) {
-    if (!st || !out) return MXQ_ERR_INVALID_ARG;
+// Validation and view logic shared by the single and grouped exports: fills
+// `c` and reports whether a copy is needed (rows * nb bytes).
+static mxq_status export_plan(const mxq_mxfp8_storage* st, mxq_mxfp8_components* c, bool* copy) {
+    if (!st) return MXQ_ERR_INVALID_ARG;
     if (!valid_shape(st->rows, st->K, st->K) || !valid_layout(st->lay)) return MXQ_ERR_INVALID_ARG;
     if (st->fp8 != MXQ_E4M3 && st->fp8 != MXQ_E5M2) return MXQ_ERR_INVALID_ARG;
     const int64_t nb = (st->K + 31) / 32;
     const bool empty = st->rows == 0 || st->K == 0;
     if (!st->data && !empty) return MXQ_ERR_NO_ROWWISE_DATA;
     if (!st->scales && !empty) return MXQ_ERR_INVALID_ARG;
-    mxq_mxfp8_components c{};
-    c.data = st->data;
-    c.fp8 = st->fp8;
-    c.rows = st->rows;
-    c.K = st->K;
-    c.scale_cols = nb;
+    *c = mxq_mxfp8_components{};
+    c->data = st->data;
+    c->fp8 = st->fp8;
+    c->rows = st->rows;
+    c->K = st->K;
+    c->scale_cols = nb;
     const bool view = st->lay == MXQ_SCALES_COMPACT || (st->lay == MXQ_SCALES_PADDED && nb % 4 == 0);
-    if (empty || view) {
-        c.scales = st->scales;
-        c.is_view = 1;
+    *copy = !(empty || view);
+    if (!*copy) {
+        c->scales = st->scales;
+        c->is_view = 1;
+    }
+    return MXQ_OK;
+}
+
+mxq_status mxq_export_mxfp8(const mxq_mxfp8_storage* st, uint8_t* scale_out, size_t scale_out_bytes,
+                            mxq_mxfp8_components* out, cudaStream_t stream) {
+    if (!st || !out) return MXQ_ERR_INVALID_ARG;
+    mxq_mxfp8_components c;
+    bool copy = false;
+    mxq_status s = export_plan(st, &c, &copy);
+    if (s != MXQ_OK) return s;
+    if (!copy) {
         *out = c;
         return MXQ_OK;
     }
-    if (!scale_out || scale_out_bytes < (size_t)(st->rows * nb)) return MXQ_ERR_BUFFER_TOO_SMALL;
+    if (!scale_out || scale_out_bytes < (size_t)(st->rows * c.scale_cols)) return MXQ_ERR_BUFFER_TOO_SMALL;
     mxq::ExportArgs a{};
     a.scales = st->scales;
     a.lay = (int)st->lay;
@@ -240,6 +254,64 @@ mxq_status mxq_export_mxfp8(const mxq_mxfp8_storage* st, uint8_t* scale_out, siz
     if (ls != MXQ_OK) return ls;
     c.scales = scale_out;
     c.is_view = 0;
+    *out = c;
+    return MXQ_OK;
+}
+
+mxq_status mxq_export_mxfp8_grouped(const mxq_mxfp8_storage* st, int64_t count, uint8_t* scale_out,
+                                    size_t scale_out_bytes, mxq_mxfp8_components* out, cudaStream_t stream) {
+    if (count < 0 || (count > 0 && (!st || !out))) return MXQ_ERR_INVALID_ARG;
+    // check everything and size the copies before launching anything
+    size_t need = 0;
+    for (int64_t g = 0; g < count; ++g) {
+        mxq_mxfp8_components c;
+        bool copy = false;
+        mxq_status s = export_plan(&st[g], &c, &copy);
+        if (s != MXQ_OK) return s;
+        if (copy) need += (size_t)(st[g].rows * c.scale_cols);
+    }
+    if (need > 0 && (!scale_out || scale_out_bytes < need)) return MXQ_ERR_BUFFER_TOO_SMALL;
+    mxq::GroupedExport batch{};
+    size_t off = 0;
+    for (int64_t g = 0; g < count; ++g) {
+        mxq_mxfp8_components c;
+        bool copy = false;
+        export_plan(&st[g], &c, &copy);
+        if (copy) {
+            mxq::ExportArgs& a = batch.item[batch.count++];
+            a.scales = st[g].scales;
+            a.lay = (int)st[g].lay;
+            a.rows = st[g].rows;
+            a.K = st[g].K;
+            a.out = scale_out + off;
+            c.scales = scale_out + off;
+            c.is_view = 0;
+            off += (size_t)(st[g].rows * c.scale_cols);
+            if (batch.count == mxq::kGroupedMax) {
+                const mxq_status ls = launch_status(mxq::launch_export_grouped(batch, stream));
+                if (ls != MXQ_OK) return ls;
+                batch.count = 0;
+            }
+        }
+        out[g] = c;
+    }
+    return launch_status(mxq::launch_export_grouped(batch, stream));
+}
+
+mxq_status mxq_quantize_export_mxfp8(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                     uint8_t* data, uint8_t* scales, mxq_mxfp8_components* out, cudaStream_t stream) {
+    if (!out) return MXQ_ERR_INVALID_ARG;
+    const mxq_status s = rowwise_quant(mxq::RowMode::MXFP8, x, dt, rows, K, ldx, data, scales, MXQ_SCALES_COMPACT,
+                                       nullptr, stream);
+    if (s != MXQ_OK) return s;
+    mxq_mxfp8_components c{};
+    c.data = data;
+    c.fp8 = MXQ_E4M3;
+    c.scales = scales;
+    c.rows = rows;
+    c.K = K;
+    c.scale_cols = (K + 31) / 32;
+    c.is_view = 1;
     *out = c;
     return MXQ_OK;
 }

@@ -56,11 +56,19 @@ struct ExportArgs {
     uint8_t* out;  // compact [rows, nb]
 };
 
+// Descriptors of a grouped export, passed by value as kernel parameters.
+constexpr int kGroupedMax = 128;
+struct GroupedExport {
+    ExportArgs item[kGroupedMax];
+    int count;
+};
+
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_rowwise(RowMode mode, Elt elt, const RowwiseArgs& a, cudaStream_t s);
 cudaError_t launch_block128(Elt elt, const Block128Args& a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
 cudaError_t launch_export(const ExportArgs& a, cudaStream_t s);
+cudaError_t launch_export_grouped(const GroupedExport& b, cudaStream_t s);
 cudaError_t launch_colwise(Elt elt, const ColwiseArgs& a, cudaStream_t s);
 cudaError_t launch_colwise_dequant(const DequantArgs& a, cudaStream_t s);
 

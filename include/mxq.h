@@ -258,6 +258,29 @@ typedef struct {
 MXQ_API mxq_status mxq_export_mxfp8(const mxq_mxfp8_storage* st, uint8_t* scale_out, size_t scale_out_bytes,
                             mxq_mxfp8_components* out, cudaStream_t stream);
 
+/* Export of several storages (per-expert export; TE PR #3790 lists the
+ * per-expert export of a GroupedTensor as not covered there) in as few
+ * launches as possible: every storage is exported as by mxq_export_mxfp8;
+ * the ones that need a copy get consecutive regions of scale_out, in order,
+ * and all copies run in one kernel launch per 128 storages.
+ *   st[count], out[count]: storages and their components.
+ *   scale_out: device buffer for the copied scales, scale_out_bytes long.
+ * Errors: as mxq_export_mxfp8 for any storage (checked before anything is
+ * launched); BUFFER_TOO_SMALL if the copies do not fit. */
+MXQ_API mxq_status mxq_export_mxfp8_grouped(const mxq_mxfp8_storage* st, int64_t count, uint8_t* scale_out,
+                                            size_t scale_out_bytes, mxq_mxfp8_components* out, cudaStream_t stream);
+
+/* Quantize and export in one call (TE issue #3644: "quantize weights for
+ * inference, then extract the resulting values and scales"; TE PR #3790,
+ * Description: a standalone function that quantizes a BF16 weight first).
+ * Runs mxq_mxfp8_row_direct with COMPACT scales, which are already the
+ * exported layout, and fills `out` (a view of data and scales).
+ *   data: [rows, K] E4M3 bytes; scales: [rows, ceil(K/32)] bytes.
+ * Errors: as mxq_mxfp8_row_direct; INVALID_ARG if out is NULL. */
+MXQ_API mxq_status mxq_quantize_export_mxfp8(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                             uint8_t* data, uint8_t* scales, mxq_mxfp8_components* out,
+                                             cudaStream_t stream);
+
 /* Static description of a status code. */
 MXQ_API const char* mxq_status_string(mxq_status s);
 

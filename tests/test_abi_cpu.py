@@ -155,6 +155,19 @@ def test_export_host_logic(libs):
         st = _S(data=FAKE, scales=FAKE + 4096, fp8=0, lay=lay, rows=100, K=48)
         assert L.mxq_export_mxfp8(ctypes.byref(st), None, 0, ctypes.byref(c), None) == TOO_SMALL
         assert L.mxq_export_mxfp8(ctypes.byref(st), FAKE, 199, ctypes.byref(c), None) == TOO_SMALL
+    # grouped: every storage is checked before anything launches
+    L.mxq_export_mxfp8_grouped.argtypes = [ctypes.POINTER(_S), ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
+                                           ctypes.POINTER(_C), ctypes.c_void_p]
+    arr = (_S * 3)(_S(data=FAKE, scales=FAKE, fp8=0, lay=0, rows=4, K=32),
+                   _S(data=FAKE, scales=FAKE, fp8=0, lay=2, rows=100, K=48),
+                   _S(data=None, scales=FAKE, fp8=0, lay=0, rows=4, K=32))
+    comps = (_C * 3)()
+    assert L.mxq_export_mxfp8_grouped(arr, 3, FAKE, 1 << 20, comps, None) == NO_ROWWISE
+    assert L.mxq_export_mxfp8_grouped(arr, 2, FAKE, 199, comps, None) == TOO_SMALL
+    assert L.mxq_export_mxfp8_grouped(arr, 1, None, 0, comps, None) == OK  # a view: nothing to copy
+    assert comps[0].is_view == 1 and comps[0].scales == FAKE
+    assert L.mxq_export_mxfp8_grouped(arr, 0, None, 0, comps, None) == OK
+    assert L.mxq_export_mxfp8_grouped(arr, -1, None, 0, comps, None) == INVALID
     # empty storage exports as an empty view even without data
     st = _S(data=None, scales=None, fp8=0, lay=2, rows=0, K=48)
     assert L.mxq_export_mxfp8(ctypes.byref(st), None, 0, ctypes.byref(c), None) == OK
