@@ -433,6 +433,53 @@ def test_moe_expert_stack_export(mx):
         np.testing.assert_array_equal(host_bits(comp.scale_inv[e][rows]), rs)
 
 
+# ---------------------------------------------------------- size limits
+
+def test_grid_loops_past_65535_row_tiles(mx):
+    """8,388,736 x 32 bf16: 65,537 tiles of 128 rows and 262,148 bands of 32
+    rows, more than one grid dimension holds, so the blockwise, columnwise
+    and export kernels loop over their grid; sampled tile bands and the
+    last rows against the oracle."""
+    rows, K = 65537 * 128, 32
+    base = syn.normal_bf16(4096, K, seed=61)
+    x = dev_bf16(base).repeat(rows // 4096 + 1, 1)[:rows].contiguous()
+    bd, bs = mx.fp8_block128_direct(x)
+    cd, cs = mx.mxfp8_col_direct(x, "compact")
+    d, s = mx.mxfp8_row_direct(x, "swizzled")
+    comp = mx.export_mxfp8(d, s, shape=x.shape, layout="swizzled")
+    torch.cuda.synchronize()
+    for band in (0, 4095, 65536):
+        r0 = band * 128
+        xb = np.concatenate([base, base])[r0 % 4096:r0 % 4096 + 128]
+        rd, rs = oracle.fp8_block128_direct(xb)
+        np.testing.assert_array_equal(host_bits(bd[r0:r0 + 128]), rd)
+        assert int(host_bits(bs[band])[0]) == int(rs.view(np.uint32)[0, 0])
+        cdd, css = oracle.mxfp8_col_direct(xb)
+        np.testing.assert_array_equal(host_bits(cd[r0:r0 + 128]), cdd)
+        np.testing.assert_array_equal(host_bits(cs[:, 4 * band:4 * band + 4]), css)
+        _, rcs = oracle.mxfp8_row_direct(xb)
+        np.testing.assert_array_equal(host_bits(comp.scale_inv[r0:r0 + 128]), rcs)
+
+
+def test_tensor_over_4gib_sampled(mx):
+    """A 65536 x 40960 bf16 weight (5.4 GB, 2.7e9 elements): projection and
+    MXFP8 rowwise, sampled rows against the oracle (64-bit offsets)."""
+    rows, K = 65536, 40960
+    base = syn.normal_bf16(256, K, seed=62)
+    x = dev_bf16(base).repeat(rows // 256, 1)
+    y = mx.fake_quant_mxfp4(x)
+    d, s = mx.mxfp8_row_direct(x, "compact")
+    torch.cuda.synchronize()
+    for r in (0, 255, 40000, 65535):
+        xr = base[r % 256:r % 256 + 1]
+        np.testing.assert_array_equal(host_bits(y[r:r + 1]), oracle.fake_quant_mxfp4(xr))
+        rd, rs = oracle.mxfp8_row_direct(xr)
+        np.testing.assert_array_equal(host_bits(d[r:r + 1]), rd)
+        np.testing.assert_array_equal(host_bits(s[r:r + 1]), rs)
+    del x, y, d, s
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------- grouped export, quantize+export
 
 def test_grouped_export_matches_single_exports(mx):
