@@ -7,12 +7,20 @@
 // round-up power of two: s = ceil(log2(amax / 448)) clamped to [-127, 127]
 // (zero amax: -127), payloads RTNE_E4M3(y / 2^s).
 //
-// One CTA per 32-row band x 256 columns: warp w owns the 32x32 tile of
-// columns 32w.., lane t its row.  The lane projects its 1x32 row block in
-// registers (the projection never goes back to HBM), stages it in a padded
-// shared tile, reads its column back for the 32x1 amax and exponent, and
-// then encodes its row with the 32 column scales -- one 32-byte payload
-// store per lane.  Only __syncwarp() between the steps.
+// bf16 with 32-byte aligned rows and K % 32 == 0 (tile64_kernel): a warp owns
+// a 32-row band x 64 columns.  Four lanes share a row, each with a 16-column
+// chunk, so one 32-byte load per lane covers eight whole 128-byte lines and
+// each row's two 1x32 blocks are read with full lines (a lane-per-row layout
+// touches 32 half lines per load, which the L1 pays for).  A block's two
+// lanes join their amax with one shuffle; each lane projects its chunks in
+// registers (the projection never goes back to HBM) and stages them in a
+// padded shared tile; lane t then scans the column pair (2t, 2t+1) over the
+// 32 rows with the packed NaN-propagating abs-max, and the lanes encode their
+// chunks with the bf16 multipliers 2^-s of the columns -- an exact product,
+// as the projected value has two significant bits -- and the E4M3 conversion.
+// Registers are capped at 64 so that 32 warps stay resident per SM.
+// Other views (fp32, unaligned or ragged K) use colwise_kernel: a warp per
+// 32-row band x 32 columns, a lane per row, the same steps.
 #include <cuda_runtime.h>
 
 #include "mxq_device.cuh"
@@ -52,6 +60,27 @@ __device__ __forceinline__ int host_exponent(uint32_t amax_mag) {
     int s = E - 135 + (frac > (3u << (MANT - 2)) ? 1 : 0);
     s = E == 0 ? -127 : s;
     return min(max(s, -127), 127);
+}
+
+// Zero the padding of a padded / swizzled (transposed, K x ceil(rows/32))
+// scale buffer: thread p of `stride` threads takes entries p, p + stride, ...
+__device__ __forceinline__ void zero_scale_padding(const ColwiseArgs& a, int64_t p0, int64_t stride) {
+    const int64_t nbr = (a.rows + 31) >> 5, Cpt = (nbr + 3) & ~int64_t(3);
+    const int64_t Rp = (a.K + 127) & ~int64_t(127);
+    const int64_t extra = Cpt - nbr;
+    const int64_t padA = a.K * extra, padB = (Rp - a.K) * Cpt;
+    for (int64_t p = p0; p < padA + padB; p += stride) {
+        int64_t rr, jj;
+        if (p < padA) {
+            rr = p / extra;
+            jj = nbr + (p - rr * extra);
+        } else {
+            const int64_t q = p - padA;
+            rr = a.K + q / Cpt;
+            jj = q - (rr - a.K) * Cpt;
+        }
+        a.scales[scale_offset(rr, jj, nbr, Cpt, a.lay)] = 0;
+    }
 }
 
 template <Elt ELT, bool VEC, int DST>
@@ -234,24 +263,125 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(ColwiseArgs a, int64_
         __syncwarp();  // the tile is rewritten by the next band
     }
 
-    if (a.lay != 0 && blockIdx.y == 0) {
-        // zero the padding of the padded / swizzled (transposed) scale buffer
-        const int64_t Rp = (a.K + 127) & ~int64_t(127);
-        const int64_t extra = Cpt - nbr;
-        const int64_t padA = a.K * extra, padB = (Rp - a.K) * Cpt;
-        for (int64_t p = (int64_t)blockIdx.x * kThreads + threadIdx.x; p < padA + padB; p += (int64_t)gridDim.x * kThreads) {
-            int64_t rr, jj;
-            if (p < padA) {
-                rr = p / extra;
-                jj = nbr + (p - rr * extra);
+    if (a.lay != 0 && blockIdx.y == 0) zero_scale_padding(a, (int64_t)blockIdx.x * kThreads + threadIdx.x,
+                                                          (int64_t)gridDim.x * kThreads);
+}
+
+// E4M3 conversion of two fp32 values into one 16-bit half, and two halves
+// into a word.
+__device__ __forceinline__ uint16_t e4m3x2_h(uint32_t hi, uint32_t lo) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "r"(hi), "r"(lo));
+    return d;
+}
+__device__ __forceinline__ uint32_t pack_halves(uint16_t lo, uint16_t hi) {
+    uint32_t d;
+    asm("mov.b32 %0, {%1, %2};" : "=r"(d) : "h"(lo), "h"(hi));
+    return d;
+}
+
+// bf16 2^-s (s in [-127, 127]: a normal, or the subnormal 2^-127); NaN for
+// a poisoned column block, so that its payloads convert to 0x7F.
+__device__ __forceinline__ uint32_t bf16_col_multiplier(uint32_t cm, int sx) {
+    if (cm >= 0x7F80u) return 0x7FC0u;
+    return sx <= 126 ? (uint32_t)(127 - sx) << 7 : 0x0040u;
+}
+
+constexpr int kTileWarps = 2;
+
+__global__ void __launch_bounds__(32 * kTileWarps, 16) tile64_kernel(ColwiseArgs a, int64_t bands) {
+    constexpr int RW = 32 + 4;  // words per staged row: 64 bf16 + 16 B pad (conflict-free 16-byte stores)
+    __shared__ __align__(16) uint32_t tile[kTileWarps][32 * RW];
+    __shared__ __align__(16) uint32_t colmul[kTileWarps][32];
+    const int w = threadIdx.x >> 5, t = threadIdx.x & 31, q = t & 3, g = t >> 2;
+    const int64_t nbr = (a.rows + 31) >> 5, Cpt = (nbr + 3) & ~int64_t(3);
+    const int64_t col0 = ((int64_t)blockIdx.x * kTileWarps + w) * 64;  // first column of the warp tile
+    const bool cvalid = col0 + 16 * q < a.K;                             // this lane's chunk is in the tensor
+    const int64_t c0 = col0 + 2 * t;                                     // the column pair this lane scans
+    uint32_t* trow = tile[w] + g * RW + 8 * q;
+
+    for (int64_t band = blockIdx.y; band < bands; band += gridDim.y) {
+        const int64_t rbase = band * 32 + g;  // rows rbase + 8i, i = 0..3
+        const char* xp = static_cast<const char*>(a.x) + (rbase * a.ldx + col0 + 16 * q) * 2;
+        const int64_t xstep = 16 * a.ldx;  // 8 rows, in bytes
+        uint32_t y[4][8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (cvalid && rbase + 8 * i < a.rows) {
+                ld32(y[i], xp + i * xstep);
             } else {
-                const int64_t q = p - padA;
-                rr = a.K + q / Cpt;
-                jj = q - (rr - a.K) * Cpt;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) y[i][k] = 0u;  // +0 adds nothing to an amax
             }
-            a.scales[scale_offset(rr, jj, nbr, Cpt, a.lay)] = 0;
         }
+        // projection, one chunk at a time (same rule and arithmetic as mxq_fake_quant_mxfp4)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t m = 0u;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m = bf2_absmax(m, y[i][k]);
+            m &= 0x7FFF7FFFu;
+            m = max(m & 0xFFFFu, m >> 16);
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));  // the block's other half
+            const int e = block_exponent<7>(m);
+            const Bf16Grid gr = bf16_grid_unit(e);
+            const uint32_t scl = bf16_pow2_pair(e);
+            if (e != 125) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) y[i][k] = bf2_mul(bf2_grid(y[i][k], gr) | (y[i][k] & 0x80008000u), scl);
+            } else {  // the upper clamp: saturate at +-6; a NaN or Inf block poisons its outputs
+                const bool pois = m >= 0x7F80u;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t u = bf2_sat(bf2_grid(y[i][k], gr) | (y[i][k] & 0x80008000u), 0x40C040C0u);
+                    y[i][k] = pois ? 0x7FC07FC0u : bf2_mul(u, scl);
+                }
+            }
+            uint32_t* d = trow + 8 * i * RW;
+            *reinterpret_cast<uint4*>(d) = make_uint4(y[i][0], y[i][1], y[i][2], y[i][3]);
+            *reinterpret_cast<uint4*>(d + 4) = make_uint4(y[i][4], y[i][5], y[i][6], y[i][7]);
+        }
+        __syncwarp();
+
+        // 32x1 maxima of the column pair (2t, 2t+1) and their scales
+        uint32_t m2 = 0u;
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) m2 = bf2_absmax(m2, tile[w][rr * RW + t]);
+        m2 &= 0x7FFF7FFFu;
+        const uint32_t cm0 = m2 & 0xFFFFu, cm1 = m2 >> 16;
+        const int sx0 = host_exponent<7>(cm0), sx1 = host_exponent<7>(cm1);
+        colmul[w][t] = bf16_col_multiplier(cm0, sx0) | (bf16_col_multiplier(cm1, sx1) << 16);
+        if (band < nbr) {
+            if (c0 < a.K) a.scales[scale_offset(c0, band, nbr, Cpt, a.lay)] = (uint8_t)(cm0 >= 0x7F80u ? 255 : sx0 + 127);
+            if (c0 + 1 < a.K)
+                a.scales[scale_offset(c0 + 1, band, nbr, Cpt, a.lay)] = (uint8_t)(cm1 >= 0x7F80u ? 255 : sx1 + 127);
+        }
+        __syncwarp();
+
+        // encode: the lane's chunk columns 16q.. have the multiplier words 8q..8q+7
+        const uint4 ma = *reinterpret_cast<const uint4*>(&colmul[w][8 * q]);
+        const uint4 mb = *reinterpret_cast<const uint4*>(&colmul[w][8 * q + 4]);
+        const uint32_t mul[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+        uint8_t* dp = a.data + rbase * a.K + col0 + 16 * q;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t* d = trow + 8 * i * RW;
+            const uint4 ya = *reinterpret_cast<const uint4*>(d), yb = *reinterpret_cast<const uint4*>(d + 4);
+            const uint32_t yy[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
+            uint32_t b[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t z0 = bf2_mul(yy[2 * u], mul[2 * u]);
+                const uint32_t z1 = bf2_mul(yy[2 * u + 1], mul[2 * u + 1]);
+                b[u] = pack_halves(e4m3x2_h(z0 & 0xFFFF0000u, z0 << 16), e4m3x2_h(z1 & 0xFFFF0000u, z1 << 16));
+            }
+            if (cvalid && rbase + 8 * i < a.rows) st16(dp + 8 * i * a.K, b[0], b[1], b[2], b[3]);
+        }
+        __syncwarp();  // the tile is rewritten by the next band
     }
+
+    if (a.lay != 0 && blockIdx.y == 0) zero_scale_padding(a, (int64_t)blockIdx.x * blockDim.x + threadIdx.x,
+                                                          (int64_t)gridDim.x * blockDim.x);
 }
 
 // Dequantize of the columnwise form: out[r, c] = payload * 2^(code(c, r/32) - 127).
@@ -308,6 +438,12 @@ cudaError_t dispatch(const ColwiseArgs& a, cudaStream_t s) {
     const bool vec = aligned(a.x, 32) && (a.ldx * es) % 32 == 0 && (a.K * es) % 32 == 0;
     const int dst = (aligned(a.data, 32) && a.K % 32 == 0) ? 2 : (aligned(a.data, 16) && a.K % 16 == 0) ? 1 : 0;
     if (!vec) return launch_one<ELT, false, 0>(a, s);
+    if (ELT == Elt::BF16 && a.K % 32 == 0 && aligned(a.data, 16)) {
+        const int64_t bands = ceil_div(a.rows, 32), gx = ceil_div(ceil_div(a.K, 64), kTileWarps);
+        const unsigned gy = (unsigned)(bands < 65535 ? bands : 65535);
+        tile64_kernel<<<dim3((unsigned)gx, gy), 32 * kTileWarps, 0, s>>>(a, bands);
+        return cudaGetLastError();
+    }
     if (dst == 2) return launch_one<ELT, true, 2>(a, s);
     if (dst == 1) return launch_one<ELT, true, 1>(a, s);
     return launch_one<ELT, true, 0>(a, s);
