@@ -265,6 +265,9 @@ def run_gpu(args, rank, world):
     # end to end through the public API: pinned host weight in, every result back to pinned host memory
     e2e = None if args.no_e2e else run_e2e(args, lib, dev, x_host, world)
 
+    # the MoE expert stack: MXFP8 rowwise into swizzled scales, then export to compact
+    moe = None if args.no_moe else run_moe(args, lib, dev, stream, world)
+
     if rank != 0:
         return None
     peak, peak_src = load_peaks()
@@ -293,10 +296,90 @@ def run_gpu(args, rank, world):
                      "algorithmic_bytes": BYTES[dom]},
         "clocks": clk.result,
         "e2e": e2e,
+        "moe": moe,
         "gpu_launches": len(names) * args.steps,
         "timing": "CUDA events on the launch stream; steps replay one CUDA graph per input rotation (5 launches "
                   "each); per_conversion replays per-kernel graphs of back-to-back launches",
     }
+
+
+def run_moe(args, lib, dev, stream, world):
+    """32 experts x 4096 x 7184 bf16 (K % 32 = 16: 225 scale columns, padded
+    to 228), each expert N(0, 0.02) * 2^U{-8..8} from its own seed.  Times
+    the MXFP8 rowwise conversion of the whole stack into GEMM-swizzled scales
+    (one launch, 2.8 GB of traffic, larger than L2) and the export of those
+    scales to compact (8 rotating copies of the 29.9 MB swizzled buffer, so
+    reads come from HBM)."""
+    import concurrent.futures as cf
+
+    import torch
+
+    from block_scaled_precision_x32_gb300 import synthetic as syn
+
+    E, Rw, K = syn.MOE_EXPERTS, syn.MOE_ROWS, syn.MOE_K
+    rows, nb = E * Rw, -(-K // 32)
+    x = torch.empty((E, Rw, K), dtype=torch.bfloat16, device=dev)
+    with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        for e, h in enumerate(ex.map(syn.moe_expert_bf16, range(E))):
+            x[e].copy_(torch.from_numpy(h.view(np.int16)).view(torch.bfloat16))
+    sbytes = lib.scale_bytes(rows, K, "swizzled")
+    data = torch.empty((E, Rw, K), dtype=torch.uint8, device=dev)
+    R = 8
+    sw = [torch.empty(sbytes, dtype=torch.uint8, device=dev) for _ in range(R)]
+    out = torch.empty(rows * nb, dtype=torch.uint8, device=dev)
+    # prepared calls captured into CUDA graphs (as for the 8192 x 8192 step), so
+    # host launch overhead stays out of the timed loop
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        row = lib.plan_mxfp8_row_direct(x, "swizzled", data, sw[0])
+        row()
+        for i in range(1, R):
+            sw[i].copy_(sw[0])
+        exports = [lib.plan_export_mxfp8(data, sw[i], shape=(E, Rw, K), layout="swizzled", scale_out=out)[0]
+                   for i in range(R)]
+        for c in exports:
+            c()
+        side.synchronize()
+        g_row, g_ex = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_row, stream=side):
+            row()
+        with torch.cuda.graph(g_ex, stream=side):
+            for c in exports:
+                c()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    g_row.replay()
+    g_ex.replay()
+    torch.cuda.synchronize()
+
+    def timed(fn, reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(a.elapsed_time(b), world) / reps
+
+    row_reps = max(3, min(50, args.steps // 40))
+    ex_reps = max(1, min(200, args.steps // 10))
+    row_ms = timed(g_row.replay, row_reps)
+    ex_ms = timed(g_ex.replay, ex_reps) / R
+    peak, _ = load_peaks()
+    row_bytes = 3 * rows * K + sbytes
+    ex_bytes = sbytes + rows * nb
+    del x, data, sw, g_row, g_ex
+    torch.cuda.empty_cache()
+
+    def rec(ms, nbytes):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"us": round(ms * 1e3, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nbytes}
+
+    return {"workload": f"MoE expert stack {E}x{Rw}x{K} bf16, N(0,0.02)*2^U{{-8..8}} per expert (synthetic)",
+            "mxfp8_row_swizzled": rec(row_ms, row_bytes), "export_swizzled_to_compact": rec(ex_ms, ex_bytes),
+            "reps": {"mxfp8_row": row_reps, "export": ex_reps * R}}
 
 
 def run_e2e(args, lib, dev, x_host, world, chunks: int = 8):
@@ -501,6 +584,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["mxq", "reference"], default="mxq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--no-moe", action="store_true", help="skip the MoE expert-stack measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -11,6 +11,9 @@
 // padded by one word so that lanes reading the same word of consecutive
 // tiles hit distinct banks -- and written out row by row, consecutive lanes
 // on consecutive output words (4 scales) or bytes.
+// Swizzled input with nb % 4 != 0 (compact rows are not whole words): one CTA
+// per 128-row tile stages all of the tile's column tiles, and writes the
+// tile's compact output -- one contiguous range -- as aligned words.
 // Padded input: one warp per row, lanes on consecutive bytes.
 // Grouped export: up to kGroupedMax storages per launch, their descriptors
 // passed by value in the kernel parameters.
@@ -27,6 +30,56 @@ constexpr int kThreads = 256;
 constexpr int kGroup = 32;        // column tiles (4 scale columns each) per CTA
 constexpr int kTileWords = 129;   // 128 words of a 512-byte tile + 1 pad word
 
+// Stage `ntiles` consecutive 512-byte swizzled tiles from `src` into `tile`
+// (kTileWords words per tile).  Each thread issues up to kStageBatch loads
+// before its first shared-memory store, so the loads of a thread overlap
+// instead of paying one memory latency each.
+constexpr int kStageBatch = 8;
+
+template <bool VEC_IN, int BATCH = kStageBatch>
+__device__ __forceinline__ void stage_tiles(const uint8_t* src, int ntiles, uint32_t* tile) {
+    if constexpr (VEC_IN) {
+        const int n = ntiles * 32;  // 16-byte chunks
+        for (int base = 0; base < n; base += BATCH * kThreads) {
+            uint4 q[BATCH];
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) {
+                const int i = base + u * kThreads + (int)threadIdx.x;
+                if (i < n) q[u] = reinterpret_cast<const uint4*>(src)[i];
+            }
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) {
+                const int i = base + u * kThreads + (int)threadIdx.x;
+                if (i < n) {
+                    uint32_t* d = tile + (i >> 5) * kTileWords + (i & 31) * 4;
+                    d[0] = q[u].x;
+                    d[1] = q[u].y;
+                    d[2] = q[u].z;
+                    d[3] = q[u].w;
+                }
+            }
+        }
+    } else {
+        const int n = ntiles * 128;  // words
+        for (int base = 0; base < n; base += BATCH * kThreads) {
+            uint32_t wv[BATCH];
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) {
+                const int i = base + u * kThreads + (int)threadIdx.x;
+                if (i < n) {
+                    const uint8_t* b = src + 4 * i;
+                    wv[u] = b[0] | ((uint32_t)b[1] << 8) | ((uint32_t)b[2] << 16) | ((uint32_t)b[3] << 24);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) {
+                const int i = base + u * kThreads + (int)threadIdx.x;
+                if (i < n) tile[(i >> 7) * kTileWords + (i & 127)] = wv[u];
+            }
+        }
+    }
+}
+
 // One (128-row tile rt, group of column tiles starting at jt0) of a
 // swizzled scale buffer -> compact rows.  `tile` is the CTA's staging area.
 template <bool VEC_IN, bool WORD_OUT>
@@ -36,23 +89,7 @@ __device__ __forceinline__ void unswizzle_group(const ExportArgs& a, int64_t rt,
     const int64_t ct = Cp >> 2;  // column tiles per row tile
     const int g = (int)min((int64_t)kGroup, ct - jt0);
     const int W = (int)min((int64_t)4 * g, nb - 4 * jt0);  // output columns of this group
-    const uint8_t* src = a.scales + (rt * ct + jt0) * 512;
-    if constexpr (VEC_IN) {
-        for (int i = threadIdx.x; i < g * 32; i += kThreads) {
-            const uint4 q = reinterpret_cast<const uint4*>(src)[i];
-            uint32_t* d = tile + (i >> 5) * kTileWords + (i & 31) * 4;
-            d[0] = q.x;
-            d[1] = q.y;
-            d[2] = q.z;
-            d[3] = q.w;
-        }
-    } else {
-        for (int i = threadIdx.x; i < g * 128; i += kThreads) {
-            const uint8_t* b = src + 4 * i;
-            tile[(i >> 7) * kTileWords + (i & 127)] =
-                b[0] | ((uint32_t)b[1] << 8) | ((uint32_t)b[2] << 16) | ((uint32_t)b[3] << 24);
-        }
-    }
+    stage_tiles<VEC_IN>(a.scales + (rt * ct + jt0) * 512, g, tile);
     __syncthreads();
     const int64_t r0 = rt * 128;
     const int nrows = (int)min((int64_t)128, a.rows - r0);
@@ -79,6 +116,83 @@ __global__ void __launch_bounds__(kThreads) unswizzle_kernel(ExportArgs a, int64
     const int64_t jt0 = (int64_t)blockIdx.x * kGroup;
     for (int64_t rt = blockIdx.y; rt < tiles_r; rt += gridDim.y) unswizzle_group<VEC_IN, WORD_OUT>(a, rt, jt0, tile);
 }
+
+// Swizzled input, compact rows that are not whole words (nb % 4 != 0).
+// One CTA per 128-row tile stages the tile's ct * 512 contiguous swizzled
+// bytes.  Four consecutive compact rows starting at a multiple of 4 are
+// 4 * nb bytes = nb whole aligned words (the tile's output starts on a
+// 16-byte boundary), and every such group has the same layout, so a table
+// of nb entries -- built once per CTA, one division per entry -- says for
+// group word k which row (0..3) and row byte j its first byte is.  Word k
+// is then a funnel shift of the staged words of column tiles j/4 and
+// j/4 + 1 of that row, or, where it runs into the next row (three words
+// per group), the row's last bytes (which may also straddle two column
+// tiles) merged with the next row's first word.
+// Consecutive lanes take consecutive words: consecutive column tiles of
+// one row (distinct banks with the one-word pad), consecutive addresses.
+// (gbase[e >> 20] is the next row's column tile 0.)
+// Rows past the last whole group (only in the last tile) are byte stores;
+// so is everything when the output is not word aligned (VW == 1).
+template <int VW>
+__global__ void __launch_bounds__(kThreads) unswizzle_flat_kernel(ExportArgs a, int64_t tiles_r) {
+    // nb table entries, then ct + 1 staged tiles of kTileWords words (the
+    // spare tile lets a word read column tile j/4 + 1 unconditionally; what
+    // it holds is shifted or masked away)
+    extern __shared__ uint32_t smem[];
+    const int nb = (int)((a.K + 31) >> 5);
+    const int ct = (nb + 3) >> 2;
+    uint32_t* table = smem;
+    uint32_t* stile = smem + ((nb + 3) & ~3);
+    // Entry k: offset of the first byte's staged word from the group's row-0
+    // slot (4 r + (j/4) * kTileWords: rows 4G + r share the slot base of row
+    // 4G, as 4G + r never carries past bit 4), the byte shift j % 4, and for
+    // a word that crosses into the next row its c bytes left in the row and
+    // the next row's slot offset 4 (r + 1).
+    for (int k = threadIdx.x; k < nb; k += kThreads) {
+        const int p = 4 * k, r = p / nb, j = p - r * nb;
+        const int c = j + 4 > nb ? nb - j : 0;
+        table[k] = (uint32_t)(4 * r + (j >> 2) * kTileWords) | ((uint32_t)(j & 3) << 16) | ((uint32_t)c << 18) |
+                   ((uint32_t)(4 * (r + 1)) << 20);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t rt = blockIdx.x; rt < tiles_r; rt += gridDim.x) {
+        stage_tiles<true, 4>(a.scales + rt * ct * 512, ct, stile);
+        __syncthreads();
+        const int64_t r0 = rt * 128;
+        const int nrows = (int)min((int64_t)128, a.rows - r0);
+        uint8_t* out = a.out + r0 * nb;
+        const int groups = VW == 1 ? 0 : nrows >> 2;
+        // lane: words k = lane, lane + 32, ... of every group G = warp, warp + 8, ...
+        // of this warp; group G's row-0 slot is 16 (G % 8) + G / 8, i.e. 16 warp + i
+        // for the warp's i-th group, so the inner loop steps one word in shared
+        // memory and 8 nb words in the output.
+        uint32_t* const o0 = reinterpret_cast<uint32_t*>(out) + (int64_t)warp * nb;
+        const int ng = groups > warp ? (groups - warp + 7) >> 3 : 0;  // this warp's groups
+        for (int k = lane; k < nb; k += 32) {
+            const uint32_t e = table[k];
+            const uint32_t* pa = stile + 16 * warp + (e & 0xFFFFu);
+            const int sh = 8 * (int)((e >> 16) & 3u), c = (int)((e >> 18) & 3u);
+            uint32_t* ow = o0 + k;
+            if (c == 0) {
+                for (int i = 0; i < ng; ++i) ow[(int64_t)i * 8 * nb] = __funnelshift_r(pa[i], pa[i + kTileWords], sh);
+            } else {
+                const uint32_t* pb = stile + 16 * warp + (e >> 20);
+                const uint32_t m = (1u << (8 * c)) - 1u;
+                for (int i = 0; i < ng; ++i)
+                    ow[(int64_t)i * 8 * nb] = (__funnelshift_r(pa[i], pa[i + kTileWords], sh) & m) | (pb[i] << (8 * c));
+            }
+        }
+        // rows past the last whole group: byte stores
+        for (int f = 4 * groups * nb + (int)threadIdx.x; f < nrows * nb; f += kThreads) {
+            const int rr = f / nb, j = f - rr * nb;
+            out[f] = (uint8_t)(stile[(rr & 31) * 4 + (rr >> 5) + (j >> 2) * kTileWords] >> ((j & 3) * 8));
+        }
+        __syncthreads();  // the staged tile is rewritten by the next row tile
+    }
+}
+
+// Largest staging area of the flat kernel (bytes of dynamic shared memory).
+constexpr int kFlatSmemMax = 160 * 1024;
 
 // Rows [r0, r1) of a padded buffer -> compact; one warp per row.
 __device__ __forceinline__ void unpad_rows(const ExportArgs& a, int64_t r0, int64_t r1, int64_t warp, int64_t nwarps) {
@@ -114,15 +228,41 @@ __global__ void __launch_bounds__(kThreads) grouped_export_kernel(GroupedExport 
 
 }  // namespace
 
+namespace {
+template <int VW>
+cudaError_t launch_flat(const ExportArgs& a, int64_t tr, int64_t grid, int64_t smem, cudaStream_t s) {
+    if (smem > 48 * 1024) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(unswizzle_flat_kernel<VW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    // the kernel keeps nothing in L1: let shared memory take the whole carveout
+    const cudaError_t e = cudaFuncSetAttribute(unswizzle_flat_kernel<VW>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    unswizzle_flat_kernel<VW><<<(unsigned)grid, kThreads, (size_t)smem, s>>>(a, tr);
+    return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_export(const ExportArgs& a, cudaStream_t s) {
     const int64_t nb = ceil_div(a.K, 32);
     if (a.lay == 2) {
         const int64_t ct = ceil_div(nb, 4);
         const int64_t tr = ceil_div(a.rows, 128);
+        const bool vin = (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0;
+        const int64_t smem = (ct + 1) * kTileWords * 4 + ((nb + 3) & ~int64_t(3)) * 4;
+        // nb > 4: a word of compact output then meets at most one row boundary
+        if (nb % 4 != 0 && nb > 4 && vin && smem <= kFlatSmemMax) {
+            int64_t grid = tr;
+            const int64_t cap = (int64_t)sm_count() * 16;
+            if (grid > cap) grid = cap;
+            const uintptr_t o = reinterpret_cast<uintptr_t>(a.out);
+            return (o & 3) == 0 ? launch_flat<4>(a, tr, grid, smem, s) : launch_flat<1>(a, tr, grid, smem, s);
+        }
         const int64_t gx = ceil_div(ct, kGroup);
         const unsigned gy = (unsigned)(tr < 65535 ? tr : 65535);
         const dim3 grid((unsigned)gx, gy);
-        const bool vin = (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0;
         const bool wout = nb % 4 == 0 && (reinterpret_cast<uintptr_t>(a.out) & 3) == 0;
         if (vin && wout)
             unswizzle_kernel<true, true><<<grid, kThreads, 0, s>>>(a, tr);

@@ -502,6 +502,32 @@ def test_tensor_over_4gib_sampled(mx):
 
 # ------------------------------------------- grouped export, quantize+export
 
+@pytest.mark.parametrize("K", [32 * 1023, 32 * 1301 - 16])
+def test_export_wide_rows(mx, K):
+    """Swizzled -> compact export of rows whose scale count is not a
+    multiple of 4 and whose 128-row tile is wide: 1023 scale columns stage
+    137 KB per tile in shared memory (an opt-in size), 1301 columns exceed
+    the 160 KB cap and take the column-group kernel.  Also into a scale_out
+    that starts one byte off a word boundary (byte stores)."""
+    rows = 130
+    g = np.random.default_rng(K)
+    w = g.standard_normal((rows, K)).astype(np.float32) * np.float32(0.02)
+    w *= np.ldexp(1.0, g.integers(-20, 20, size=(rows, 1))).astype(np.float32)
+    x_np = syn.f32_to_bf16_bits(w)
+    _, ref_compact = oracle.mxfp8_row_direct(x_np, oracle.COMPACT)
+    d, s = mx.mxfp8_row_direct(dev_bf16(x_np), "swizzled")
+    nb = (K + 31) // 32
+    comp = mx.export_mxfp8(d, s, shape=(rows, K), layout="swizzled")
+    raw = torch.full((rows * nb + 8,), 0xA5, dtype=torch.uint8, device="cuda")
+    off = mx.export_mxfp8(d, s, shape=(rows, K), layout="swizzled", scale_out=raw[1:1 + rows * nb])
+    torch.cuda.synchronize()
+    want = ref_compact.reshape(rows, nb)
+    np.testing.assert_array_equal(host_bits(comp.scale_inv).reshape(rows, nb), want)
+    np.testing.assert_array_equal(host_bits(off.scale_inv).reshape(rows, nb), want)
+    r = host_bits(raw)
+    assert r[0] == 0xA5 and (r[1 + rows * nb:] == 0xA5).all()
+
+
 def test_grouped_export_matches_single_exports(mx):
     """Per-expert export of separate storages in one launch (compact view,
     padded view, padded copy, swizzled copies of different shapes) equals
