@@ -56,6 +56,7 @@ KERNEL_FILES = {
     "mxfp8_col": "mxq_colwise.cu",
     "mxfp4_pack": "mxq_rowwise.cu",
     "mxfp4_dequant_bf16": "mxq_dequant.cu",
+    "mxfp8_col_dequant_bf16": "mxq_colwise.cu",
 }
 STEP_BYTES = sum(BYTES.values())
 # Conversions beyond the five of the step, timed alone the same way.
@@ -63,6 +64,7 @@ EXTRA_BYTES = {
     "mxfp8_col": 2 * N + N + N // 32,
     "mxfp4_pack": 2 * N + N // 2 + N // 32,
     "mxfp4_dequant_bf16": N // 2 + N // 32 + 2 * N,
+    "mxfp8_col_dequant_bf16": N + N // 32 + 2 * N,
 }
 CSRC = os.path.join(ROOT, "block_scaled_precision_x32_gb300", "csrc")
 
@@ -176,6 +178,8 @@ def run_gpu(args, rank, world):
     p4_s = torch.empty(lib.scale_bytes(ROWS, COLS, "swizzled"), dtype=torch.uint8, device=dev)
     p4_in = [lib.mxfp4_pack(xs[i], "swizzled") for i in range(R)]
     p4_out = torch.empty_like(x0)
+    col_in = [lib.mxfp8_col_direct(xs[i], "swizzled") for i in range(R)]
+    col_out = torch.empty_like(x0)
     col_d = torch.empty_like(row_d)
     col_s = torch.empty(lib.scale_bytes(COLS, ROWS, "swizzled"), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
@@ -202,7 +206,9 @@ def run_gpu(args, rank, world):
             ])
         extra_plans = [[lib.plan_mxfp8_col_direct(xs[s], "swizzled", col_d, col_s),
                         lib.plan_mxfp4_pack(xs[s], "swizzled", p4, p4_s),
-                        lib.plan_dequantize(p4_in[s][0], p4_out, scales=p4_in[s][1], layout="swizzled", mxfp4=True)]
+                        lib.plan_dequantize(p4_in[s][0], p4_out, scales=p4_in[s][1], layout="swizzled", mxfp4=True),
+                        lib.plan_dequantize(col_in[s][0], col_out, scales=col_in[s][1], layout="swizzled",
+                                            columnwise=True)]
                        for s in range(R)]
         for s in range(2 * R):  # warm every launch configuration before capture
             for c in plans[s % R] + extra_plans[s % R]:

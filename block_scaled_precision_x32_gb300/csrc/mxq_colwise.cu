@@ -421,6 +421,106 @@ __global__ void __launch_bounds__(kThreads) colwise_dequant_kernel(DequantArgs a
     }
 }
 
+// Dequantize of the columnwise form, K % 32 == 0 and 32-byte aligned rows:
+// a warp owns a 32-row band x 128 columns, four lanes per row with 32
+// columns (one 32-byte payload load: a warp load covers eight whole lines).
+// The warp first turns the band's 128 column scale codes into bf16
+// multipliers 2^(code-127) in shared memory; then each element is placed
+// into a bf16 pattern as payload * 2^-120 (2^-112), multiplied exactly by
+// 2^120 (2^112) and once by its column's multiplier -- one rounding of the
+// exact product, as for the rowwise form.  A row chunk with a NaN / Inf
+// payload or a code-255 column, or (fp32 output) a column code below which
+// products leave bf16's normal range, takes the element-wise fp32 path.
+template <bool E5M2, bool BF16OUT>
+__global__ void __launch_bounds__(kThreads, 4) colwise_dequant_tile_kernel(DequantArgs a, int64_t bands) {
+    __shared__ __align__(16) uint32_t colmul[kWarps][64];   // bf16x2 multipliers, column pairs
+    __shared__ __align__(16) uint32_t colcode[kWarps][32];  // codes, four columns per word
+    const int w = threadIdx.x >> 5, t = threadIdx.x & 31, q = t & 3, g = t >> 2;
+    const int64_t nbr = (a.rows + 31) >> 5, Cpt = (nbr + 3) & ~int64_t(3);
+    const int64_t col0 = ((int64_t)blockIdx.x * kWarps + w) * 128;
+    const bool cvalid = col0 + 32 * q < a.K;
+    constexpr uint32_t kMinCode = E5M2 ? 17u : 10u;  // fp32 output: smallest code kept on the bf16 path
+    constexpr uint32_t fix = E5M2 ? 0x77807780u : 0x7B807B80u;  // 2^112 / 2^120, both halves
+    for (int64_t band = blockIdx.y; band < bands; band += gridDim.y) {
+        uint32_t codes = 0u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t c = col0 + 4 * t + u;
+            const uint32_t code = c < a.K ? a.scales[scale_offset(c, band, nbr, Cpt, a.lay)] : 0u;
+            codes |= code << (8 * u);
+        }
+        colcode[w][t] = codes;
+        colmul[w][2 * t] = (bf16_scale_pair(codes & 0xFFu) & 0xFFFFu) | (bf16_scale_pair((codes >> 8) & 0xFFu) << 16);
+        colmul[w][2 * t + 1] =
+            (bf16_scale_pair((codes >> 16) & 0xFFu) & 0xFFFFu) | (bf16_scale_pair(codes >> 24) << 16);
+        __syncwarp();
+        // this lane's 32 columns: code words 8q.., multiplier words 16q..
+        bool colslow = false;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const uint32_t cw = colcode[w][8 * q + m];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t code = (cw >> (8 * u)) & 0xFFu;
+                colslow |= code == 255u;
+                if constexpr (!BF16OUT) colslow |= code < kMinCode;
+            }
+        }
+        for (int i = 0; i < 4; ++i) {
+            const int64_t r = band * 32 + 8 * i + g;
+            if (!cvalid || r >= a.rows) continue;
+            uint32_t pw[8];
+            ld32(pw, a.data + r * a.K + col0 + 32 * q);
+            uint32_t sp = 0u;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sp |= special_bytes<E5M2>(pw[k]);
+            char* op = static_cast<char*>(a.out) + (r * a.K + col0 + 32 * q) * (BF16OUT ? 2 : 4);
+            if (sp == 0u && !colslow) {
+#pragma unroll
+                for (int s8 = 0; s8 < (BF16OUT ? 2 : 4); ++s8) {
+                    uint32_t seg[8];
+#pragma unroll
+                    for (int v = 0; v < (BF16OUT ? 8 : 4); ++v) {
+                        const int pidx = (BF16OUT ? 8 : 4) * s8 + v;  // column pair within the chunk
+                        const uint32_t pr = place_pair<E5M2>(pw[pidx >> 1], (pidx & 1) ? 0x4342u : 0x4140u);
+                        const uint32_t y = bf2_mul(bf2_mul(pr, fix), colmul[w][16 * q + pidx]);
+                        if constexpr (BF16OUT) {
+                            seg[v] = y;
+                        } else {
+                            seg[2 * v] = y << 16;
+                            seg[2 * v + 1] = y & 0xFFFF0000u;
+                        }
+                    }
+                    st32(op + 32 * s8, seg);
+                }
+            } else {
+#pragma unroll 1
+                for (int s8 = 0; s8 < (BF16OUT ? 2 : 4); ++s8) {
+                    uint32_t seg[8];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        uint32_t o = 0u;
+#pragma unroll
+                        for (int hh = 0; hh < (BF16OUT ? 2 : 1); ++hh) {
+                            const int e = BF16OUT ? 16 * s8 + 2 * v + hh : 8 * s8 + v;  // element of the chunk
+                            const uint32_t code = (colcode[w][8 * q + (e >> 2)] >> (8 * (e & 3))) & 0xFFu;
+                            const uint32_t scale = code == 255u ? 0x7FC00000u : f32_pow2((int)code - 127);
+                            const uint32_t f = decode_scaled<E5M2>((pw[e >> 2] >> (8 * (e & 3))) & 0xFFu, scale);
+                            if constexpr (BF16OUT)
+                                o |= bf16_rne(f) << (16 * hh);
+                            else
+                                o = f;
+                        }
+                        seg[v] = o;
+                    }
+                    st32(op + 32 * s8, seg);
+                }
+            }
+        }
+        __syncwarp();  // colmul / colcode are rewritten by the next band
+    }
+}
+
 bool aligned(const void* p, int64_t n) { return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)n) == 0; }
 
 template <Elt ELT, bool VEC, int DST>
@@ -456,12 +556,24 @@ cudaError_t launch_colwise(Elt elt, const ColwiseArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_colwise_dequant(const DequantArgs& a, cudaStream_t s) {
+    const bool e5 = a.fp8 == 1;
+    const int oes = a.out_bf16 ? 2 : 4;
+    if (a.K % 32 == 0 && aligned(a.data, 32) && aligned(a.out, 32) && (a.K * oes) % 32 == 0) {
+        const int64_t bands = ceil_div(a.rows, 32), gx = ceil_div(ceil_div(a.K, 128), kWarps);
+        const dim3 grid((unsigned)gx, (unsigned)(bands < 65535 ? bands : 65535));
+        if (e5)
+            a.out_bf16 ? colwise_dequant_tile_kernel<true, true><<<grid, kThreads, 0, s>>>(a, bands)
+                       : colwise_dequant_tile_kernel<true, false><<<grid, kThreads, 0, s>>>(a, bands);
+        else
+            a.out_bf16 ? colwise_dequant_tile_kernel<false, true><<<grid, kThreads, 0, s>>>(a, bands)
+                       : colwise_dequant_tile_kernel<false, false><<<grid, kThreads, 0, s>>>(a, bands);
+        return cudaGetLastError();
+    }
     const int64_t total = ceil_div(a.rows, 32) * a.K;
     int64_t grid = ceil_div(total, (int64_t)kThreads);
     const int64_t cap = (int64_t)sm_count() * 8;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    const bool e5 = a.fp8 == 1;
     if (e5)
         a.out_bf16 ? colwise_dequant_kernel<true, true><<<(unsigned)grid, kThreads, 0, s>>>(a)
                    : colwise_dequant_kernel<true, false><<<(unsigned)grid, kThreads, 0, s>>>(a);

@@ -40,46 +40,6 @@ __device__ __forceinline__ int64_t scale_offset(int64_t r, int64_t j, int64_t nb
     return ((r >> 7) * (Cp >> 2) + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
 }
 
-// fp8 byte -> exact fp32 pattern times `scale` (IEEE fp32 product), NaN made canonical.
-template <bool E5M2>
-__device__ __forceinline__ uint32_t decode_scaled(uint32_t b, uint32_t scale) {
-    const uint32_t mag = b & 0x7Fu;
-    uint32_t f;
-    bool nan;
-    if constexpr (E5M2) {
-        f = f32_mul((mag << 21) | ((b & 0x80u) << 24), 0x77800000u);  // * 2^112
-        nan = mag > 0x7Cu;
-        if (mag == 0x7Cu) f = 0x7F800000u | ((b & 0x80u) << 24);
-    } else {
-        f = f32_mul((mag << 20) | ((b & 0x80u) << 24), 0x7B800000u);  // * 2^120
-        nan = mag == 0x7Fu;
-    }
-    const uint32_t r = f32_mul(f, scale);
-    return (nan || (r & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FC00000u : r;
-}
-
-// fp32 pattern -> bf16 pattern, round to nearest even (canonical NaN stays
-// canonical, overflow goes to Inf).
-__device__ __forceinline__ uint32_t bf16_rne(uint32_t u) { return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16; }
-
-// Any byte of w a NaN/Inf payload?  (E4M3: low 7 bits all ones; E5M2:
-// exponent all ones.)
-template <bool E5M2>
-__device__ __forceinline__ uint32_t special_bytes(uint32_t w) {
-    if constexpr (E5M2)
-        return ((w & 0x7C7C7C7Cu) + 0x04040404u) & 0x80808080u;
-    else
-        return ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
-}
-
-// Payload bytes (lo, hi) of one word's pair -> bf16x2 of payload * 2^-120 / 2^-112.
-template <bool E5M2>
-__device__ __forceinline__ uint32_t place_pair(uint32_t w, uint32_t sel) {
-    const uint32_t t = prmt(w, 0u, sel);  // byte k of the pair at bits 16k..16k+7
-    constexpr int SH = E5M2 ? 5 : 4;
-    return ((t & 0x007F007Fu) << SH) | ((t & 0x00800080u) << 8);
-}
-
 template <int SRC>
 __device__ __forceinline__ void load_payload(uint32_t (&w)[8], const uint8_t* p, int valid) {
     if constexpr (SRC == 2) {
@@ -185,7 +145,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a, int64_
             // of 0, .5, 1, 1.5, 2, 3, 4, 6) indexed by PRMT, signs spread by one
             // multiply, then one exact bf16 multiply by 2^(code-127) (Inf past
             // bf16's range, as rounding the exact fp32 product would give).
-            const uint32_t scale16 = c == 0u ? 0x00400040u : ((c << 7) | (c << 23));
+            const uint32_t scale16 = bf16_scale_pair(c);
             uint32_t o[WORDS];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -229,7 +189,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a, int64_
 #pragma unroll
             for (int k = 0; k < 8; ++k) sp |= special_bytes<E5M2>(w[k]);
             fast = sp == 0u && c != 255u && (BF16OUT || c >= (E5M2 ? 17u : 10u));
-            scale16 = c == 0u ? 0x00400040u : ((c << 7) | (c << 23));
+            scale16 = bf16_scale_pair(c);
         } else {
             scale32 = reinterpret_cast<const uint32_t*>(a.tile_scale_inv)[(r >> 7) * tc + (col0 >> 7)];
         }

@@ -203,4 +203,51 @@ __device__ __forceinline__ uint32_t f32_pow2(int k) {  // 2^k, k in [-127, 127]
     return k >= -126 ? (uint32_t)(k + 127) << 23 : 0x00400000u;
 }
 
+// ------------------------------------------------------ fp8 payload decode
+
+// fp8 byte -> exact fp32 pattern times `scale` (IEEE fp32 product), NaN made canonical.
+template <bool E5M2>
+__device__ __forceinline__ uint32_t decode_scaled(uint32_t b, uint32_t scale) {
+    const uint32_t mag = b & 0x7Fu;
+    uint32_t f;
+    bool nan;
+    if constexpr (E5M2) {
+        f = f32_mul((mag << 21) | ((b & 0x80u) << 24), 0x77800000u);  // * 2^112
+        nan = mag > 0x7Cu;
+        if (mag == 0x7Cu) f = 0x7F800000u | ((b & 0x80u) << 24);
+    } else {
+        f = f32_mul((mag << 20) | ((b & 0x80u) << 24), 0x7B800000u);  // * 2^120
+        nan = mag == 0x7Fu;
+    }
+    const uint32_t r = f32_mul(f, scale);
+    return (nan || (r & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FC00000u : r;
+}
+
+// fp32 pattern -> bf16 pattern, round to nearest even (canonical NaN stays
+// canonical, overflow goes to Inf).
+__device__ __forceinline__ uint32_t bf16_rne(uint32_t u) { return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16; }
+
+// Any byte of w a NaN/Inf payload?  (E4M3: low 7 bits all ones; E5M2:
+// exponent all ones.)
+template <bool E5M2>
+__device__ __forceinline__ uint32_t special_bytes(uint32_t w) {
+    if constexpr (E5M2)
+        return ((w & 0x7C7C7C7Cu) + 0x04040404u) & 0x80808080u;
+    else
+        return ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+}
+
+// Payload bytes (lo, hi) of one word's pair -> bf16x2 of payload * 2^-120 / 2^-112.
+template <bool E5M2>
+__device__ __forceinline__ uint32_t place_pair(uint32_t w, uint32_t sel) {
+    const uint32_t t = prmt(w, 0u, sel);  // byte k of the pair at bits 16k..16k+7
+    constexpr int SH = E5M2 ? 5 : 4;
+    return ((t & 0x007F007Fu) << SH) | ((t & 0x00800080u) << 8);
+}
+
+// bf16x2 2^(code - 127) for a UE8M0 code in 0..254 (code 0: the bf16 subnormal 2^-127).
+__device__ __forceinline__ uint32_t bf16_scale_pair(uint32_t code) {
+    return code == 0u ? 0x00400040u : ((code << 7) | (code << 23));
+}
+
 }  // namespace mxq

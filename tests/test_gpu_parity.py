@@ -296,6 +296,31 @@ def test_dequant_every_payload_and_scale_code(mx, lay, kind):
         np.testing.assert_array_equal(host_bits(got), oracle_bits(oracle.dequant_mxfp8(data, compact, oracle.COMPACT, kind, ocode)))
 
 
+@pytest.mark.parametrize("K", [256, 272])
+@pytest.mark.parametrize("lay", LAYOUTS)
+@pytest.mark.parametrize("kind", [oracle.E4M3, oracle.E5M2])
+def test_dequant_columnwise_every_payload_and_scale_code(mx, K, lay, kind):
+    """Columnwise form: every payload byte in every column, each column with
+    its own scale codes (all 256 codes appear, 255 and the small codes that
+    leave bf16's normal range for fp32 output included); K = 256 takes the
+    warp-tile kernel, K = 272 the element-wise one; 100 rows end in a
+    ragged band."""
+    rows = 100
+    g = np.random.default_rng(K * 10 + kind * 3 + lay)
+    data = np.tile(np.arange(256, dtype=np.uint8), (rows, 2))[:, :K].copy()
+    g.shuffle(data, axis=1)
+    nbr = (rows + 31) // 32
+    cs = ((np.arange(K)[:, None] * 37 + np.arange(nbr)[None, :] * 101) % 256).astype(np.uint8)  # K x nbr codes
+    scales = cs.reshape(-1) if lay == oracle.COMPACT else oracle.scales_to_layout(cs, K, rows, lay)
+    d = torch.from_numpy(data).cuda()
+    s = torch.from_numpy(scales).cuda()
+    for odt, ocode in ((torch.float32, oracle.FP32), (torch.bfloat16, oracle.BF16)):
+        got = mx.dequantize(d, scales=s, layout=lay, fp8="e4m3" if kind == oracle.E4M3 else "e5m2", out_dtype=odt,
+                            columnwise=True)
+        want = oracle.dequant_mxfp8(np.ascontiguousarray(data.T), cs, oracle.COMPACT, kind, ocode).T
+        np.testing.assert_array_equal(host_bits(got), oracle_bits(np.ascontiguousarray(want)))
+
+
 def test_dequant_block128_arbitrary_scales(mx):
     """Blockwise dequantize with scale_inv that are not powers of two
     (rounded fp32 products, subnormal results, overflow to Inf)."""
