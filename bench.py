@@ -523,6 +523,33 @@ def cpu_baseline(budget_s: float = 15.0):
                       f"single-threaded C oracle, {tot_t:.1f} s"}
 
 
+def _oracle_slab(task):
+    cols, seed = task
+    return oracle_sample(cols, seed=seed)
+
+
+def cpu_baseline_all_cores(budget_s: float = 10.0):
+    """The same oracle on every host core at once: one process per core
+    (spawned, so no CUDA state is inherited), each converting its own
+    128-row slabs.  Throughput = all slabs' bytes / wall time of the pool's
+    work (pool start-up and imports excluded by a warm-up task per worker)."""
+    import multiprocessing as mp
+
+    n = os.cpu_count() or 1
+    cols = _cols_for(budget_s / 2)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(n) as pool:
+        pool.map(_oracle_slab, [(128, 5000 + i) for i in range(n)])  # start every worker, load the oracle
+        tasks = [(cols, 1003 + i) for i in range(2 * n)]
+        t = time.perf_counter()
+        res = pool.map(_oracle_slab, tasks, chunksize=1)
+        wall = time.perf_counter() - t
+    nbytes = sum(b for _, b in res)
+    return {"value": round(nbytes / wall / 1e9, 5), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{len(tasks)} slabs of 128 x {cols} of the bf16 weight over {n} processes (one per core), "
+                      f"whole step (5 conversions) each, the single-threaded C oracle unchanged, {wall:.1f} s wall"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -605,6 +632,7 @@ def main(argv=None):
     if res is not None:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline()
+            res["cpu_baseline_all_cores"] = cpu_baseline_all_cores()
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
