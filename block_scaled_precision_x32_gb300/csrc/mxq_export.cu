@@ -5,8 +5,8 @@
 // scales are copied only when padded in the last dimension or swizzled for
 // GEMM, padding dropped and the swizzle undone.
 //
-// Swizzled input: one CTA per (128-row tile, group of 32 column tiles).
-// The group's bytes are contiguous in the swizzled buffer (32 x 512), so
+// Swizzled input: one CTA per (128-row tile, group of 16 column tiles).
+// The group's bytes are contiguous in the swizzled buffer (16 x 512), so
 // they are staged in shared memory with 16-byte loads -- each 512-byte tile
 // padded by one word so that lanes reading the same word of consecutive
 // tiles hit distinct banks -- and written out row by row, consecutive lanes
@@ -27,7 +27,7 @@ namespace mxq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kGroup = 32;        // column tiles (4 scale columns each) per CTA
+constexpr int kGroup = 16;        // column tiles (4 scale columns each) per CTA: 3.6 us at 8192^2 against 4.1 for 32
 constexpr int kTileWords = 129;   // 128 words of a 512-byte tile + 1 pad word
 
 // Stage `ntiles` consecutive 512-byte swizzled tiles from `src` into `tile`
