@@ -36,20 +36,20 @@ constexpr int kTileWords = 129;   // 128 words of a 512-byte tile + 1 pad word
 // instead of paying one memory latency each.
 constexpr int kStageBatch = 8;
 
-template <bool VEC_IN, int BATCH = kStageBatch>
+template <bool VEC_IN, int BATCH = kStageBatch, int NT = kThreads>
 __device__ __forceinline__ void stage_tiles(const uint8_t* src, int ntiles, uint32_t* tile) {
     if constexpr (VEC_IN) {
         const int n = ntiles * 32;  // 16-byte chunks
-        for (int base = 0; base < n; base += BATCH * kThreads) {
+        for (int base = 0; base < n; base += BATCH * NT) {
             uint4 q[BATCH];
 #pragma unroll
             for (int u = 0; u < BATCH; ++u) {
-                const int i = base + u * kThreads + (int)threadIdx.x;
+                const int i = base + u * NT + (int)threadIdx.x;
                 if (i < n) q[u] = reinterpret_cast<const uint4*>(src)[i];
             }
 #pragma unroll
             for (int u = 0; u < BATCH; ++u) {
-                const int i = base + u * kThreads + (int)threadIdx.x;
+                const int i = base + u * NT + (int)threadIdx.x;
                 if (i < n) {
                     uint32_t* d = tile + (i >> 5) * kTileWords + (i & 31) * 4;
                     d[0] = q[u].x;
@@ -61,11 +61,11 @@ __device__ __forceinline__ void stage_tiles(const uint8_t* src, int ntiles, uint
         }
     } else {
         const int n = ntiles * 128;  // words
-        for (int base = 0; base < n; base += BATCH * kThreads) {
+        for (int base = 0; base < n; base += BATCH * NT) {
             uint32_t wv[BATCH];
 #pragma unroll
             for (int u = 0; u < BATCH; ++u) {
-                const int i = base + u * kThreads + (int)threadIdx.x;
+                const int i = base + u * NT + (int)threadIdx.x;
                 if (i < n) {
                     const uint8_t* b = src + 4 * i;
                     wv[u] = b[0] | ((uint32_t)b[1] << 8) | ((uint32_t)b[2] << 16) | ((uint32_t)b[3] << 24);
@@ -73,7 +73,7 @@ __device__ __forceinline__ void stage_tiles(const uint8_t* src, int ntiles, uint
             }
 #pragma unroll
             for (int u = 0; u < BATCH; ++u) {
-                const int i = base + u * kThreads + (int)threadIdx.x;
+                const int i = base + u * NT + (int)threadIdx.x;
                 if (i < n) tile[(i >> 7) * kTileWords + (i & 127)] = wv[u];
             }
         }
@@ -133,8 +133,11 @@ __global__ void __launch_bounds__(kThreads) unswizzle_kernel(ExportArgs a, int64
 // (gbase[e >> 20] is the next row's column tile 0.)
 // Rows past the last whole group (only in the last tile) are byte stores;
 // so is everything when the output is not word aligned (VW == 1).
+constexpr int kFlatThreads = 256;
+
 template <int VW>
-__global__ void __launch_bounds__(kThreads) unswizzle_flat_kernel(ExportArgs a, int64_t tiles_r) {
+__global__ void __launch_bounds__(kFlatThreads) unswizzle_flat_kernel(ExportArgs a, int64_t tiles_r) {
+    constexpr int NW = kFlatThreads / 32;  // warps; a multiple of 8
     // nb table entries, then ct + 1 staged tiles of kTileWords words (the
     // spare tile lets a word read column tile j/4 + 1 unconditionally; what
     // it holds is shifted or masked away)
@@ -148,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) unswizzle_flat_kernel(ExportArgs a, 
     // 4G, as 4G + r never carries past bit 4), the byte shift j % 4, and for
     // a word that crosses into the next row its c bytes left in the row and
     // the next row's slot offset 4 (r + 1).
-    for (int k = threadIdx.x; k < nb; k += kThreads) {
+    for (int k = threadIdx.x; k < nb; k += kFlatThreads) {
         const int p = 4 * k, r = p / nb, j = p - r * nb;
         const int c = j + 4 > nb ? nb - j : 0;
         table[k] = (uint32_t)(4 * r + (j >> 2) * kTileWords) | ((uint32_t)(j & 3) << 16) | ((uint32_t)c << 18) |
@@ -156,34 +159,38 @@ __global__ void __launch_bounds__(kThreads) unswizzle_flat_kernel(ExportArgs a, 
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int64_t rt = blockIdx.x; rt < tiles_r; rt += gridDim.x) {
-        stage_tiles<true, 4>(a.scales + rt * ct * 512, ct, stile);
+        stage_tiles<true, 4, kFlatThreads>(a.scales + rt * ct * 512, ct, stile);
         __syncthreads();
         const int64_t r0 = rt * 128;
         const int nrows = (int)min((int64_t)128, a.rows - r0);
         uint8_t* out = a.out + r0 * nb;
         const int groups = VW == 1 ? 0 : nrows >> 2;
-        // lane: words k = lane, lane + 32, ... of every group G = warp, warp + 8, ...
-        // of this warp; group G's row-0 slot is 16 (G % 8) + G / 8, i.e. 16 warp + i
-        // for the warp's i-th group, so the inner loop steps one word in shared
-        // memory and 8 nb words in the output.
+        // lane: words k = lane, lane + 32, ... of every group G = warp + NW i of this
+        // warp; group G's row-0 slot is 16 (G % 8) + G / 8 = 16 (warp % 8) + warp / 8
+        // + (NW / 8) i, so the inner loop steps NW / 8 words in shared memory and
+        // NW nb words in the output.
         uint32_t* const o0 = reinterpret_cast<uint32_t*>(out) + (int64_t)warp * nb;
-        const int ng = groups > warp ? (groups - warp + 7) >> 3 : 0;  // this warp's groups
+        const int ng = groups > warp ? (groups - warp + NW - 1) / NW : 0;  // this warp's groups
+        const uint32_t* const wbase = stile + 16 * (warp & 7) + (warp >> 3);
+        constexpr int ds = NW / 8;
         for (int k = lane; k < nb; k += 32) {
             const uint32_t e = table[k];
-            const uint32_t* pa = stile + 16 * warp + (e & 0xFFFFu);
+            const uint32_t* pa = wbase + (e & 0xFFFFu);
             const int sh = 8 * (int)((e >> 16) & 3u), c = (int)((e >> 18) & 3u);
             uint32_t* ow = o0 + k;
             if (c == 0) {
-                for (int i = 0; i < ng; ++i) ow[(int64_t)i * 8 * nb] = __funnelshift_r(pa[i], pa[i + kTileWords], sh);
+                for (int i = 0; i < ng; ++i)
+                    ow[(int64_t)i * NW * nb] = __funnelshift_r(pa[ds * i], pa[ds * i + kTileWords], sh);
             } else {
-                const uint32_t* pb = stile + 16 * warp + (e >> 20);
+                const uint32_t* pb = wbase + (e >> 20);
                 const uint32_t m = (1u << (8 * c)) - 1u;
                 for (int i = 0; i < ng; ++i)
-                    ow[(int64_t)i * 8 * nb] = (__funnelshift_r(pa[i], pa[i + kTileWords], sh) & m) | (pb[i] << (8 * c));
+                    ow[(int64_t)i * NW * nb] =
+                        (__funnelshift_r(pa[ds * i], pa[ds * i + kTileWords], sh) & m) | (pb[ds * i] << (8 * c));
             }
         }
         // rows past the last whole group: byte stores
-        for (int f = 4 * groups * nb + (int)threadIdx.x; f < nrows * nb; f += kThreads) {
+        for (int f = 4 * groups * nb + (int)threadIdx.x; f < nrows * nb; f += kFlatThreads) {
             const int rr = f / nb, j = f - rr * nb;
             out[f] = (uint8_t)(stile[(rr & 31) * 4 + (rr >> 5) + (j >> 2) * kTileWords] >> ((j & 3) * 8));
         }
@@ -240,7 +247,7 @@ cudaError_t launch_flat(const ExportArgs& a, int64_t tr, int64_t grid, int64_t s
     const cudaError_t e = cudaFuncSetAttribute(unswizzle_flat_kernel<VW>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                                (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    unswizzle_flat_kernel<VW><<<(unsigned)grid, kThreads, (size_t)smem, s>>>(a, tr);
+    unswizzle_flat_kernel<VW><<<(unsigned)grid, kFlatThreads, (size_t)smem, s>>>(a, tr);
     return cudaGetLastError();
 }
 }  // namespace
