@@ -483,13 +483,14 @@ def test_moe_expert_stack_export(mx):
 def test_grid_loops_past_65535_row_tiles(mx):
     """8,388,736 x 32 bf16: 65,537 tiles of 128 rows and 262,148 bands of 32
     rows, more than one grid dimension holds, so the blockwise, columnwise
-    and export kernels loop over their grid; sampled tile bands and the
-    last rows against the oracle."""
+    (conversion and dequantize) and export kernels loop over their grid;
+    sampled tile bands against the oracle."""
     rows, K = 65537 * 128, 32
     base = syn.normal_bf16(4096, K, seed=61)
     x = dev_bf16(base).repeat(rows // 4096 + 1, 1)[:rows].contiguous()
     bd, bs = mx.fp8_block128_direct(x)
     cd, cs = mx.mxfp8_col_direct(x, "compact")
+    cdq = mx.dequantize(cd, scales=cs, layout="compact", out_dtype=torch.bfloat16, columnwise=True)
     d, s = mx.mxfp8_row_direct(x, "swizzled")
     comp = mx.export_mxfp8(d, s, shape=x.shape, layout="swizzled")
     torch.cuda.synchronize()
@@ -502,8 +503,29 @@ def test_grid_loops_past_65535_row_tiles(mx):
         cdd, css = oracle.mxfp8_col_direct(xb)
         np.testing.assert_array_equal(host_bits(cd[r0:r0 + 128]), cdd)
         np.testing.assert_array_equal(host_bits(cs[:, 4 * band:4 * band + 4]), css)
+        want = oracle.dequant_mxfp8(np.ascontiguousarray(cdd.T), css, oracle.COMPACT, oracle.E4M3, oracle.BF16).T
+        np.testing.assert_array_equal(host_bits(cdq[r0:r0 + 128]), oracle_bits(np.ascontiguousarray(want)))
         _, rcs = oracle.mxfp8_row_direct(xb)
         np.testing.assert_array_equal(host_bits(comp.scale_inv[r0:r0 + 128]), rcs)
+
+
+def test_export_word_store_kernel_loops_over_row_tiles(mx):
+    """320,000 x 160 bf16 (5 scale columns): 2500 row tiles, more than the
+    word-store export kernel's resident grid, so its CTAs loop; the export
+    equals the compact scales over the whole tensor and sampled rows,
+    the last 1000 included, match the oracle."""
+    rows, K = 2500 * 128, 160
+    base = syn.normal_bf16(1000, K, seed=63)
+    x = dev_bf16(base).repeat(rows // 1000, 1).contiguous()
+    d, s = mx.mxfp8_row_direct(x, "swizzled")
+    _, sc = mx.mxfp8_row_direct(x, "compact")
+    comp = mx.export_mxfp8(d, s, shape=x.shape, layout="swizzled")
+    torch.cuda.synchronize()
+    assert torch.equal(comp.scale_inv.reshape(-1), sc.reshape(-1))
+    _, ref = oracle.mxfp8_row_direct(base)
+    got = host_bits(comp.scale_inv).reshape(rows, -1)
+    for r0 in (0, 1000 * 137, rows - 1000):
+        np.testing.assert_array_equal(got[r0:r0 + 1000], ref)
 
 
 def test_tensor_over_4gib_sampled(mx):
