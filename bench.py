@@ -274,6 +274,9 @@ def run_gpu(args, rank, world):
     # the MoE expert stack: MXFP8 rowwise into swizzled scales, then export to compact
     moe = None if args.no_moe else run_moe(args, lib, dev, stream, world)
 
+    # the same conversions of an fp32 weight (fp32 master weights)
+    fp32 = None if args.no_fp32 else run_fp32(args, lib, dev, stream, world)
+
     if rank != 0:
         return None
     peak, peak_src = load_peaks()
@@ -303,6 +306,7 @@ def run_gpu(args, rank, world):
         "clocks": clk.result,
         "e2e": e2e,
         "moe": moe,
+        "fp32": fp32,
         "gpu_launches": len(names) * args.steps,
         "timing": "CUDA events on the launch stream; steps replay one CUDA graph per input rotation (5 launches "
                   "each); per_conversion replays per-kernel graphs of back-to-back launches",
@@ -386,6 +390,72 @@ def run_moe(args, lib, dev, stream, world):
     return {"workload": f"MoE expert stack {E}x{Rw}x{K} bf16, N(0,0.02)*2^U{{-8..8}} per expert (synthetic)",
             "mxfp8_row_swizzled": rec(row_ms, row_bytes), "export_swizzled_to_compact": rec(ex_ms, ex_bytes),
             "reps": {"mxfp8_row": row_reps, "export": ex_reps * R}}
+
+
+def run_fp32(args, lib, dev, stream, world):
+    """The step's conversions and the columnwise / packed forms of an
+    8192 x 8192 fp32 weight (N(0, 0.02), seed 1003), three rotating copies
+    (800 MB, beyond L2), each conversion a CUDA graph of back-to-back
+    launches timed with events."""
+    import torch
+
+    from block_scaled_precision_x32_gb300 import synthetic as syn
+
+    R = 3
+    w = syn.normal_bf16(ROWS, COLS, seed=syn.SEED_BASE + 3)  # the bf16 weight, widened exactly to fp32
+    x0 = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).to(dev).float()
+    xs = [x0.clone() for _ in range(R)]
+    del x0
+    y = torch.empty_like(xs[0])
+    rd = torch.empty((ROWS, COLS), dtype=torch.uint8, device=dev)
+    rs = torch.empty(lib.scale_bytes(ROWS, COLS, "swizzled"), dtype=torch.uint8, device=dev)
+    bd = torch.empty_like(rd)
+    bs = torch.empty(lib.tile_scale_count(ROWS, COLS), dtype=torch.float32, device=dev)
+    cd = torch.empty_like(rd)
+    cs = torch.empty(lib.scale_bytes(COLS, ROWS, "swizzled"), dtype=torch.uint8, device=dev)
+    pk = torch.empty((ROWS, COLS // 2), dtype=torch.uint8, device=dev)
+    ps = torch.empty_like(rs)
+    conv = {
+        "projection": (lambda x: lib.plan_fake_quant_mxfp4(x, y), 8 * N),
+        "mxfp8_row": (lambda x: lib.plan_mxfp8_row_direct(x, "swizzled", rd, rs), 5 * N + N // 32),
+        "block128": (lambda x: lib.plan_fp8_block128_direct(x, bd, bs), 5 * N + 4 * (ROWS // 128) * (COLS // 128)),
+        "mxfp8_col": (lambda x: lib.plan_mxfp8_col_direct(x, "swizzled", cd, cs), 5 * N + N // 32),
+        "mxfp4_pack": (lambda x: lib.plan_mxfp4_pack(x, "swizzled", pk, ps), 4 * N + N // 2 + N // 32),
+    }
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    graphs = {}
+    with torch.cuda.stream(side):
+        for nm, (mk, nbytes) in conv.items():
+            calls = [mk(x) for x in xs]
+            for c in calls:
+                c()
+            side.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for c in calls:
+                    c()
+            graphs[nm] = (g, nbytes)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    peak, _ = load_peaks()
+    reps = max(3, min(100, args.steps // 20))
+    out = {"workload": "8192x8192 fp32 weight (the bench weight widened), 3 rotating copies"}
+    for nm, (g, nbytes) in graphs.items():
+        g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(a.elapsed_time(b), world) / (reps * R)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[nm] = {"us": round(ms * 1e3, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nbytes}
+    del xs, graphs
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, lib, dev, x_host, world, chunks: int = 8):
@@ -618,6 +688,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--no-moe", action="store_true", help="skip the MoE expert-stack measurement")
+    ap.add_argument("--no-fp32", action="store_true", help="skip the fp32-weight measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
