@@ -73,6 +73,120 @@ __device__ __forceinline__ void load_blk(uint32_t (&v)[T128<ELT>::SEGS][8], cons
     }
 }
 
+// Block exponent of one block (e = clamp(ceil(log2(amax / 6)), -126, 125))
+// and whether a NaN / Inf poisons it.
+template <Elt ELT>
+__device__ __forceinline__ int block_exp(const uint32_t (&v)[T128<ELT>::SEGS][8], bool& pois) {
+    using P = T128<ELT>;
+    uint32_t m = 0u;
+    if constexpr (ELT == Elt::BF16) {
+#pragma unroll
+        for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m = bf2_absmax(m, v[s][k]);
+        m &= 0x7FFF7FFFu;
+        m = max(m & 0xFFFFu, m >> 16);
+        pois = m >= 0x7F80u;
+    } else {
+#pragma unroll
+        for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m = f32_absmax(m, v[s][k]);
+        m &= 0x7FFFFFFFu;
+        pois = m >= 0x7F800000u;
+    }
+    return block_exponent<P::MANT>(m);
+}
+
+// Encode one block of a tile with tile exponent T and store its 32 payload
+// bytes at d (valid of them).
+template <Elt ELT, int DST>
+__device__ __forceinline__ void encode_block(const uint32_t (&v)[T128<ELT>::SEGS][8], int eb, int T, bool pois,
+                                             int valid, uint8_t* d) {
+    using P = T128<ELT>;
+    // RTNE onto E4M3 of p * 2^(e_b - T): the grid value p is exact in
+    // bf16/fp32, the power-of-two fold is exact in fp32 (or far below
+    // E4M3's smallest subnormal), and cvt rounds once.
+    const uint32_t fold = f32_pow2(max(eb - T, -126));
+    const bool top = eb == 125;  // only there can |x| / 2^e round past 6
+    uint32_t b[8];
+    if constexpr (ELT == Elt::BF16) {
+        if (T <= 6 && eb - T >= -4) {
+            // Every nonzero payload p * 2^(e_b - T) is >= 2^-5, an E4M3
+            // normal, so the encode is exact: round onto the grid in the
+            // domain z = x * 2^(-T - 120), where the bf16 exponent field of a
+            // value equals its E4M3 one and bits 10..4 are the E4M3 byte.
+            Bf16Grid g;
+            g.mult = bf16_pow2_pair(-T - 120);
+            g.floor = bf16_pow2_pair(eb - T - 120);
+#pragma unroll
+            for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t w0 = v[s][2 * q], w1 = v[s][2 * q + 1];
+                    const uint32_t t0 = bf2_grid(w0, g), t1 = bf2_grid(w1, g);
+                    b[4 * s + q] = lop_select(prmt(t0 >> 4, t1 >> 4, 0x6420u), prmt(w0, w1, 0x7531u), 0x7F7F7F7Fu);
+                }
+        } else {
+            const Bf16Grid g = bf16_grid_unit(eb);
+#pragma unroll
+            for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t h[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t w = v[s][2 * q + u];
+                        uint32_t t = bf2_grid(w, g);
+                        if (top) t = bf2_sat(t, 0x40C040C0u);
+                        const uint32_t sg = t | (w & 0x80008000u);
+                        h[u] = e4m3x2_from_f32(f32_mul(sg & 0xFFFF0000u, fold), f32_mul(sg << 16, fold));
+                    }
+                    b[4 * s + q] = h[0] | (h[1] << 16);
+                }
+        }
+    } else if (eb - T >= -5) {
+        // every nonzero payload p * 2^(e_b - T) is an exact E4M3 normal: E2M1
+        // codes by the hardware conversion, bytes from a table
+        const uint32_t mult = f32_pow2(-eb);
+        const E4m3Table tab = e4m3_table(eb - T);
+#pragma unroll
+        for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+                b[2 * s + q] = e4m3x4_from_grid(v[s][4 * q], v[s][4 * q + 1], v[s][4 * q + 2], v[s][4 * q + 3], mult, tab);
+    } else {
+        const uint32_t mult = f32_pow2(-eb);
+#pragma unroll
+        for (int s = 0; s < P::SEGS; ++s)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint32_t u4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t w = v[s][4 * q + u];
+                    uint32_t tt = f32_grid(w, mult);
+                    if (top) tt = f32_sat(tt);
+                    u4[u] = f32_mul(tt | (w & 0x80000000u), fold);
+                }
+                b[2 * s + q] = e4m3x2_from_f32(u4[1], u4[0]) | (e4m3x2_from_f32(u4[3], u4[2]) << 16);
+            }
+    }
+    if (pois)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) b[k] = 0x7F7F7F7Fu;
+    if constexpr (DST == 2) {
+        st32(d, b);
+    } else if constexpr (DST == 1) {
+        st16(d, b[0], b[1], b[2], b[3]);
+        if (valid > 16) st16(d + 16, b[4], b[5], b[6], b[7]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            if (k < valid) d[k] = (uint8_t)(b[k >> 2] >> ((k & 3) * 8));
+    }
+}
+
 template <Elt ELT, bool VEC, int DST>
 __global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB)
     block128_kernel(Block128Args a, int64_t tiles_r, int64_t tiles_c) {
@@ -100,24 +214,7 @@ __global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB)
             xp[i] = static_cast<const char*>(a.x) + (row * a.ldx + col0) * P::ES;
             uint32_t v[P::SEGS][8];
             load_blk<ELT, VEC, 1>(v, xp[i], valid[i]);
-            uint32_t m = 0u;
-            if constexpr (ELT == Elt::BF16) {
-#pragma unroll
-                for (int s = 0; s < P::SEGS; ++s)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) m = bf2_absmax(m, v[s][k]);
-                m &= 0x7FFF7FFFu;
-                m = max(m & 0xFFFFu, m >> 16);
-                pois[i] = m >= 0x7F80u;
-            } else {
-#pragma unroll
-                for (int s = 0; s < P::SEGS; ++s)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) m = f32_absmax(m, v[s][k]);
-                m &= 0x7FFFFFFFu;
-                pois[i] = m >= 0x7F800000u;
-            }
-            eb[i] = block_exponent<P::MANT>(m);
+            eb[i] = block_exp<ELT>(v, pois[i]);
             if (!pois[i] && valid[i] > 0) local = max(local, eb[i]);
             if constexpr (kHold) {
 #pragma unroll
@@ -150,80 +247,86 @@ __global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB)
             } else {
                 load_blk<ELT, VEC, 2>(v, xp[i], valid[i]);
             }
-            // RTNE onto E4M3 of p * 2^(e_b - T): the grid value p is exact in
-            // bf16/fp32, the power-of-two fold is exact in fp32 (or far below
-            // E4M3's smallest subnormal), and cvt rounds once.
-            const uint32_t fold = f32_pow2(max(eb[i] - T, -126));
-            const bool top = eb[i] == 125;  // only there can |x| / 2^e round past 6
-            uint32_t b[8];
-            if constexpr (ELT == Elt::BF16) {
-                if (T <= 6 && eb[i] - T >= -4) {
-                    // Every nonzero payload p * 2^(e_b - T) is >= 2^-5, an E4M3
-                    // normal, so the encode is exact: round onto the grid in the
-                    // domain z = x * 2^(-T - 120), where the bf16 exponent field of a
-                    // value equals its E4M3 one and bits 10..4 are the E4M3 byte.
-                    Bf16Grid g;
-                    g.mult = bf16_pow2_pair(-T - 120);
-                    g.floor = bf16_pow2_pair(eb[i] - T - 120);
-#pragma unroll
-                    for (int s = 0; s < P::SEGS; ++s)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint32_t w0 = v[s][2 * q], w1 = v[s][2 * q + 1];
-                            const uint32_t t0 = bf2_grid(w0, g), t1 = bf2_grid(w1, g);
-                            b[4 * s + q] = lop_select(prmt(t0 >> 4, t1 >> 4, 0x6420u), prmt(w0, w1, 0x7531u), 0x7F7F7F7Fu);
-                        }
-                } else {
-                    const Bf16Grid g = bf16_grid_unit(eb[i]);
-#pragma unroll
-                    for (int s = 0; s < P::SEGS; ++s)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t h[2];
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const uint32_t w = v[s][2 * q + u];
-                                uint32_t t = bf2_grid(w, g);
-                                if (top) t = bf2_sat(t, 0x40C040C0u);
-                                const uint32_t sg = t | (w & 0x80008000u);
-                                h[u] = e4m3x2_from_f32(f32_mul(sg & 0xFFFF0000u, fold), f32_mul(sg << 16, fold));
-                            }
-                            b[4 * s + q] = h[0] | (h[1] << 16);
-                        }
-                }
-            } else {
-                const uint32_t mult = f32_pow2(-eb[i]);
-#pragma unroll
-                for (int s = 0; s < P::SEGS; ++s)
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        uint32_t u4[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const uint32_t w = v[s][4 * q + u];
-                            uint32_t tt = f32_grid(w, mult);
-                            if (top) tt = f32_sat(tt);
-                            u4[u] = f32_mul(tt | (w & 0x80000000u), fold);
-                        }
-                        b[2 * s + q] = e4m3x2_from_f32(u4[1], u4[0]) | (e4m3x2_from_f32(u4[3], u4[2]) << 16);
-                    }
-            }
-            if (pois[i])
-#pragma unroll
-                for (int k = 0; k < 8; ++k) b[k] = 0x7F7F7F7Fu;
             const int q = i * P::NT + t;
-            uint8_t* d = a.data + (ti * 128 + (q >> 2)) * a.K + tj * 128 + (q & 3) * 32;
-            if constexpr (DST == 2) {
-                st32(d, b);
-            } else if constexpr (DST == 1) {
-                st16(d, b[0], b[1], b[2], b[3]);
-                if (valid[i] > 16) st16(d + 16, b[4], b[5], b[6], b[7]);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if (k < valid[i]) d[k] = (uint8_t)(b[k >> 2] >> ((k & 3) * 8));
-            }
+            encode_block<ELT, DST>(v, eb[i], T, pois[i], valid[i],
+                                   a.data + (ti * 128 + (q >> 2)) * a.K + tj * 128 + (q & 3) * 32);
         }
+    }
+}
+
+// fp32 weights with 32-byte aligned rows and K % 32 == 0.  An fp32 tile is
+// 64 KB and a lane's block 32 registers, so only two 512-thread CTAs fit per
+// SM; a CTA that loads a tile and then converts it leaves the link idle
+// while it computes.  Here a persistent CTA stages its next tile in shared
+// memory by cp.async while it converts the current one from registers: the
+// tile is waited for, each lane copies its block into registers, the buffer
+// is refilled with the next tile, and the tile maximum and encode follow.
+// Chunk c (0..31, 16 bytes) of tile row r sits at r * 32 + (c ^ ((4 (r & 1)
+// + c / 8) & 7)): a block's eight chunks stay in its 128 bytes, and the
+// eight lanes of a quarter-warp (two rows, four blocks, one chunk each) hit
+// eight different 16-byte bank groups.
+constexpr int kPipeBytes = 128 * 512;  // one staged fp32 tile
+
+__device__ __forceinline__ int f32_slot(int r, int c) { return r * 32 + (c ^ ((4 * (r & 1) + (c >> 3)) & 7)); }
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int bytes) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gmem), "r"(bytes) : "memory");
+}
+
+__global__ void __launch_bounds__(512, 2) block128_f32_pipe_kernel(Block128Args a, int64_t tiles_r, int64_t tiles_c) {
+    using P = T128<Elt::FP32>;  // 512 threads, one block per lane
+    extern __shared__ __align__(16) uint4 stile[];  // 128 rows x 32 chunks
+    __shared__ int warp_max[P::NT / 32];
+    const int t = threadIdx.x;
+    if (a.skip != nullptr && *a.skip != 0) return;  // skip-update request: write nothing
+    const int64_t ntiles = tiles_r * tiles_c;
+    auto stage = [&](int64_t lin) {
+        const int64_t ti = lin / tiles_c, tj = lin - ti * tiles_c;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int id = m * P::NT + t, r = id >> 5, c = id & 31;
+            const int64_t row = ti * 128 + r, col = tj * 128 + c * 4;
+            const bool in = row < a.rows && col < a.K;
+            const char* src = static_cast<const char*>(a.x) + (in ? (row * a.ldx + col) * 4 : 0);
+            cp_async16(&stile[f32_slot(r, c)], src, in ? 16 : 0);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    int64_t lin = blockIdx.x;
+    if (lin < ntiles) stage(lin);
+    const int r = t >> 2, j = t & 3;  // this lane's block: tile row r, column block j
+    for (; lin < ntiles; lin += gridDim.x) {
+        const int64_t ti = lin / tiles_c, tj = lin - ti * tiles_c;
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        uint32_t v[P::SEGS][8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint4 c = stile[f32_slot(r, 8 * j + k)];
+            uint32_t* d = &v[k >> 1][(k & 1) * 4];
+            d[0] = c.x;
+            d[1] = c.y;
+            d[2] = c.z;
+            d[3] = c.w;
+        }
+        __syncthreads();  // every lane has its block: the buffer takes the next tile
+        if (lin + gridDim.x < ntiles) stage(lin + gridDim.x);
+        const int64_t row = ti * 128 + r, col0 = tj * 128 + j * 32;
+        const int valid = row < a.rows && col0 < a.K ? 32 : 0;  // K % 32 == 0: whole blocks
+        bool pois;
+        const int eb = block_exp<Elt::FP32>(v, pois);
+        int local = (!pois && valid > 0) ? eb : kNoBlock;
+        local = __reduce_max_sync(0xffffffffu, local);
+        if ((t & 31) == 0) warp_max[t >> 5] = local;
+        __syncthreads();
+        int emax = kNoBlock;
+#pragma unroll
+        for (int w = 0; w < P::NT / 32; ++w) emax = max(emax, warp_max[w]);
+        if (emax == kNoBlock) emax = -126;
+        const int T = max(emax - 6, -127);
+        if (t == 0) reinterpret_cast<uint32_t*>(a.tile_scale_inv)[ti * tiles_c + tj] = f32_pow2(T);
+        if (valid > 0) encode_block<Elt::FP32, 2>(v, eb, T, pois, valid, a.data + row * a.K + col0);
     }
 }
 
@@ -249,6 +352,18 @@ cudaError_t dispatch(const Block128Args& a, cudaStream_t s) {
     const bool vec = aligned(a.x, 32) && (a.ldx * P::ES) % 32 == 0 && (a.K * P::ES) % 32 == 0;
     const int dst = (aligned(a.data, 32) && a.K % 32 == 0) ? 2 : (aligned(a.data, 16) && a.K % 16 == 0) ? 1 : 0;
     if (!vec) return launch_one<ELT, false, 0>(a, s);
+    if (ELT == Elt::FP32 && dst == 2) {
+        const int64_t tr = ceil_div(a.rows, 128), tc = ceil_div(a.K, 128);
+        // per call: the attribute belongs to the current device
+        const cudaError_t e =
+            cudaFuncSetAttribute(block128_f32_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeBytes);
+        if (e != cudaSuccess) return e;
+        int64_t grid = tr * tc;
+        const int64_t cap = (int64_t)sm_count() * 2;  // two 512-thread CTAs per SM
+        if (grid > cap) grid = cap;
+        block128_f32_pipe_kernel<<<(unsigned)grid, T128<Elt::FP32>::NT, kPipeBytes, s>>>(a, tr, tc);
+        return cudaGetLastError();
+    }
     if (dst == 2) return launch_one<ELT, true, 2>(a, s);
     if (dst == 1) return launch_one<ELT, true, 1>(a, s);
     return launch_one<ELT, true, 0>(a, s);

@@ -203,6 +203,38 @@ __device__ __forceinline__ uint32_t f32_pow2(int k) {  // 2^k, k in [-127, 127]
     return k >= -126 ? (uint32_t)(k + 127) << 23 : 0x00400000u;
 }
 
+// ------------------------------------------- E2M1 grid -> E4M3 bytes (fp32)
+
+// Four fp32 elements x of a block with exponent e, and a payload shift d
+// in [-5, 6]: v = x * 2^-e is rounded onto the signed E2M1 grid by the
+// hardware conversion (round to nearest even -- ties to the even code --
+// saturating at +-6, the sign kept, -0 included), and each code c becomes
+// the E4M3 byte of p(c) * 2^d, every nonzero one an exact E4M3 normal.
+// The bytes come from an 8-entry table indexed by PRMT on the code's
+// magnitude: entry c is the byte of p(c) (0.5 -> 0x30 ... 6 -> 0x4C) plus
+// 8d in the exponent field; the sign goes to bit 7 through a second PRMT
+// that replicates it.
+struct E4m3Table {
+    uint32_t lo, hi;
+};
+
+__device__ __forceinline__ E4m3Table e4m3_table(int d) {
+    const uint32_t d8 = (uint32_t)(8 * d);
+    E4m3Table t;
+    t.lo = 0x3C383000u + d8 * 0x01010100u;  // codes 0..3: 0, 0.5, 1, 1.5 (code 0 stays 0)
+    t.hi = 0x4C484440u + d8 * 0x01010101u;  // codes 4..7: 2, 3, 4, 6
+    return t;
+}
+
+__device__ __forceinline__ uint32_t e4m3x4_from_grid(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, uint32_t mult,
+                                                     const E4m3Table& t) {
+    const uint32_t n = e2m1x2_from_f32(f32_mul(x1, mult), f32_mul(x0, mult)) |
+                       (e2m1x2_from_f32(f32_mul(x3, mult), f32_mul(x2, mult)) << 8);  // codes of x0..x3 in nibbles 0..3
+    const uint32_t mag = prmt(t.lo, t.hi, n & 0x7777u);
+    const uint32_t sg = ((prmt(0x80808080u, 0x80808080u, n) & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;
+    return mag | sg;
+}
+
 // ------------------------------------------------------ fp8 payload decode
 
 // fp8 byte -> exact fp32 pattern times `scale` (IEEE fp32 product), NaN made canonical.

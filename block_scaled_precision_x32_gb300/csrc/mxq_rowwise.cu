@@ -263,22 +263,16 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_
                         b[4 * s + q] = lop_select(prmt(t0 >> 4, t1 >> 4, 0x6420u), prmt(w0, w1, 0x7531u), 0x7F7F7F7Fu);
                     }
             } else {
-                const uint32_t mult = f32_pow2(-e), up = f32_pow2(shift);
-                const bool top = e == 125;
+                // payload p * 2^shift, shift in 1..6: an exact E4M3 normal; E2M1
+                // codes by the hardware conversion, bytes from a table
+                const uint32_t mult = f32_pow2(-e);
+                const E4m3Table tab = e4m3_table(shift);
 #pragma unroll
                 for (int s = 0; s < T::SEGS; ++s)
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        uint32_t p[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint32_t w = v[s][4 * q + i];
-                            uint32_t t = f32_grid(w, mult);
-                            if (top) t = f32_sat(t);
-                            p[i] = f32_mul(t, up) | (w & 0x80000000u);
-                        }
-                        b[2 * s + q] = e4m3x2_from_f32(p[1], p[0]) | (e4m3x2_from_f32(p[3], p[2]) << 16);
-                    }
+                    for (int q = 0; q < 2; ++q)
+                        b[2 * s + q] =
+                            e4m3x4_from_grid(v[s][4 * q], v[s][4 * q + 1], v[s][4 * q + 2], v[s][4 * q + 3], mult, tab);
             }
             if (poisoned)
 #pragma unroll
