@@ -315,7 +315,7 @@ def test_blockwise_exactness_boundary():
 
 def test_blockwise_clamp_and_planted_tiles():
     """Tile scale clamps at 2^-127 (fp32 0x00400000); zero, -0 and 2^-127
-    tiles (BASELINE spread-sweep workload) encode exactly."""
+    tiles (the spread-sweep workload) encode exactly."""
     x, _ = syn.spread_tiles_fp32(rows=128, K=512)
     data, sinv = oracle.fp8_block128_direct(x)
     s = sinv.view(np.uint32)
