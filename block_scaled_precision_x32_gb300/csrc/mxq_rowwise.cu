@@ -320,14 +320,17 @@ cudaError_t launch_one(const RowwiseArgs& a, cudaStream_t s) {
         if (err != cudaSuccess) return err;
         if (occ < 1) occ = 1;
     }
-    // Grid size, measured on 8192 x 8192 bf16 (a sweep of 1..12 x the resident
-    // grid and one thread per block): the projection, whose traffic is half
-    // writes, is fastest with a thread per block (41 us against 46 us for a
-    // resident grid); the read-heavy MXFP8 and MXFP4 forms with 4 x the
-    // resident grid, about two blocks per thread (32.3 / 27.1 us against
-    // 34.5 / 29.6 us resident, 34.9 / 27.7 us one per thread).
+    // Grid size, measured on 8192 x 8192 (a sweep of 1..12 x the resident grid
+    // and one thread per block): the projection, whose traffic is half writes,
+    // and every fp32 form (128 bytes per thread) are fastest with a thread per
+    // block (bf16 projection 41 us against 46 us for a resident grid; fp32
+    // MXFP8 / MXFP4 54.0 / 49.2 us against 57.3 / 52.0 us at 4 x resident);
+    // the read-heavy bf16 MXFP8 and MXFP4 forms with 4 x the resident grid,
+    // about two blocks per thread (32.3 / 27.1 us against 34.5 / 29.6 us
+    // resident, 34.9 / 27.7 us one per thread).
     int64_t grid = ceil_div(total, (int64_t)kThreads);
-    const int64_t cap = MODE == RowMode::PROJECT ? ((int64_t)1 << 30) : (int64_t)sm_count() * occ * 4;
+    const bool one_per_thread = MODE == RowMode::PROJECT || ELT == Elt::FP32;
+    const int64_t cap = one_per_thread ? ((int64_t)1 << 30) : (int64_t)sm_count() * occ * 4;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     const int64_t stride = grid * kThreads;
