@@ -7,7 +7,7 @@
 // round-up power of two: s = ceil(log2(amax / 448)) clamped to [-127, 127]
 // (zero amax: -127), payloads RTNE_E4M3(y / 2^s).
 //
-// bf16 with 32-byte aligned rows and K % 32 == 0 (tile64_kernel): a warp owns
+// 32-byte aligned rows and K % 32 == 0 (tile64_kernel, bf16 or fp32): a warp owns
 // a 32-row band x 64 columns.  Four lanes share a row, each with a 16-column
 // chunk, so one 32-byte load per lane covers eight whole 128-byte lines and
 // each row's two 1x32 blocks are read with full lines (a lane-per-row layout
@@ -19,8 +19,10 @@
 // chunks with the bf16 multipliers 2^-s of the columns -- an exact product,
 // as the projected value has two significant bits -- and the E4M3 conversion.
 // Registers are capped at 64 so that 32 warps stay resident per SM.
-// Other views (fp32, unaligned or ragged K) use colwise_kernel: a warp per
-// 32-row band x 32 columns, a lane per row, the same steps.
+// fp32 input is loaded one row chunk at a time and projected through the
+// E2M1 conversion into the same bf16 values (f32_chunk_project).  Other
+// views (unaligned, or K % 32 != 0) use colwise_kernel: a warp per 32-row
+// band x 32 columns, a lane per row, the same steps.
 #include <cuda_runtime.h>
 
 #include "mxq_device.cuh"
@@ -287,9 +289,35 @@ __device__ __forceinline__ uint32_t bf16_col_multiplier(uint32_t cm, int sx) {
     return sx <= 126 ? (uint32_t)(127 - sx) << 7 : 0x0040u;
 }
 
+// fp32 input: 16 elements of one 1x32 block (exponent e) -> the projected
+// values as 8 bf16x2 words.  E2M1 codes by the hardware conversion of
+// x * 2^-e (round to nearest even, ties to the even code, saturating at
+// +-6, sign kept); each code's grid value p as a bf16 pattern from byte
+// tables indexed by PRMT (high bytes 00 3F 3F 3F 40 40 40 40, low bytes
+// 00 00 80 C0 00 40 80 C0 for codes 0..7), the sign spread by one
+// multiply, then p * 2^e by one exact bf16 multiply: the same value as the
+// projection of the bf16 path.
+__device__ __forceinline__ void f32_chunk_project(const uint32_t (&x)[16], int e, bool pois, uint32_t (&y)[8]) {
+    const uint32_t mult = f32_pow2(-e), scl = bf16_pow2_pair(e);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint32_t n = e2m1x2_from_f32(f32_mul(x[4 * u + 1], mult), f32_mul(x[4 * u], mult)) |
+                           (e2m1x2_from_f32(f32_mul(x[4 * u + 3], mult), f32_mul(x[4 * u + 2], mult)) << 8);
+        const uint32_t sel = n & 0x7777u, sg = n & 0x8888u;
+        const uint32_t hi4 = prmt(0x3F3F3F00u, 0x40404040u, sel);
+        const uint32_t lo4 = prmt(0xC0800000u, 0xC0804000u, sel);
+        const uint32_t p0 = prmt(lo4, hi4, 0x5140u) | ((sg * 0x01001000u) & 0x80008000u);
+        const uint32_t p1 = prmt(lo4, hi4, 0x7362u) | ((sg * 0x00010010u) & 0x80008000u);
+        y[2 * u] = pois ? 0x7FC07FC0u : bf2_mul(p0, scl);
+        y[2 * u + 1] = pois ? 0x7FC07FC0u : bf2_mul(p1, scl);
+    }
+}
+
 constexpr int kTileWarps = 2;
 
+template <Elt ELT>
 __global__ void __launch_bounds__(32 * kTileWarps, 16) tile64_kernel(ColwiseArgs a, int64_t bands) {
+    constexpr int ES = ELT == Elt::BF16 ? 2 : 4;
     constexpr int RW = 32 + 4;  // words per staged row: 64 bf16 + 16 B pad (conflict-free 16-byte stores)
     __shared__ __align__(16) uint32_t tile[kTileWarps][32 * RW];
     __shared__ __align__(16) uint32_t colmul[kTileWarps][32];
@@ -302,44 +330,74 @@ __global__ void __launch_bounds__(32 * kTileWarps, 16) tile64_kernel(ColwiseArgs
 
     for (int64_t band = blockIdx.y; band < bands; band += gridDim.y) {
         const int64_t rbase = band * 32 + g;  // rows rbase + 8i, i = 0..3
-        const char* xp = static_cast<const char*>(a.x) + (rbase * a.ldx + col0 + 16 * q) * 2;
-        const int64_t xstep = 16 * a.ldx;  // 8 rows, in bytes
-        uint32_t y[4][8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (cvalid && rbase + 8 * i < a.rows) {
-                ld32(y[i], xp + i * xstep);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) y[i][k] = 0u;  // +0 adds nothing to an amax
+        const char* xp = static_cast<const char*>(a.x) + (rbase * a.ldx + col0 + 16 * q) * ES;
+        const int64_t xstep = 8 * ES * a.ldx;  // 8 rows, in bytes
+        if constexpr (ELT == Elt::FP32) {
+            // one row chunk (16 fp32, two 32-byte loads) at a time, the next one in flight
+            uint32_t x[16], nx[16];
+            const bool v0 = cvalid && rbase < a.rows;
+            if (v0) {
+                ld32(*reinterpret_cast<uint32_t(*)[8]>(&nx[0]), xp);
+                ld32(*reinterpret_cast<uint32_t(*)[8]>(&nx[8]), xp + 32);
             }
-        }
-        // projection, one chunk at a time (same rule and arithmetic as mxq_fake_quant_mxfp4)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t m = 0u;
+            for (int i = 0; i < 4; ++i) {
+                const bool vi = cvalid && rbase + 8 * i < a.rows;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) m = bf2_absmax(m, y[i][k]);
-            m &= 0x7FFF7FFFu;
-            m = max(m & 0xFFFFu, m >> 16);
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));  // the block's other half
-            const int e = block_exponent<7>(m);
-            const Bf16Grid gr = bf16_grid_unit(e);
-            const uint32_t scl = bf16_pow2_pair(e);
-            if (e != 125) {
+                for (int k = 0; k < 16; ++k) x[k] = vi ? nx[k] : 0u;  // +0 adds nothing to an amax
+                if (i < 3 && cvalid && rbase + 8 * (i + 1) < a.rows) {
+                    ld32(*reinterpret_cast<uint32_t(*)[8]>(&nx[0]), xp + (i + 1) * xstep);
+                    ld32(*reinterpret_cast<uint32_t(*)[8]>(&nx[8]), xp + (i + 1) * xstep + 32);
+                }
+                uint32_t m = 0u;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) y[i][k] = bf2_mul(bf2_grid(y[i][k], gr) | (y[i][k] & 0x80008000u), scl);
-            } else {  // the upper clamp: saturate at +-6; a NaN or Inf block poisons its outputs
-                const bool pois = m >= 0x7F80u;
+                for (int k = 0; k < 16; ++k) m = f32_absmax(m, x[k]);
+                m &= 0x7FFFFFFFu;
+                m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));  // the block's other half
+                uint32_t y[8];
+                f32_chunk_project(x, block_exponent<23>(m), m >= 0x7F800000u, y);
+                uint32_t* d = trow + 8 * i * RW;
+                *reinterpret_cast<uint4*>(d) = make_uint4(y[0], y[1], y[2], y[3]);
+                *reinterpret_cast<uint4*>(d + 4) = make_uint4(y[4], y[5], y[6], y[7]);
+            }
+        } else {
+            uint32_t y[4][8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t u = bf2_sat(bf2_grid(y[i][k], gr) | (y[i][k] & 0x80008000u), 0x40C040C0u);
-                    y[i][k] = pois ? 0x7FC07FC0u : bf2_mul(u, scl);
+            for (int i = 0; i < 4; ++i) {
+                if (cvalid && rbase + 8 * i < a.rows) {
+                    ld32(y[i], xp + i * xstep);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) y[i][k] = 0u;  // +0 adds nothing to an amax
                 }
             }
-            uint32_t* d = trow + 8 * i * RW;
-            *reinterpret_cast<uint4*>(d) = make_uint4(y[i][0], y[i][1], y[i][2], y[i][3]);
-            *reinterpret_cast<uint4*>(d + 4) = make_uint4(y[i][4], y[i][5], y[i][6], y[i][7]);
+            // projection, one chunk at a time (same rule and arithmetic as mxq_fake_quant_mxfp4)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t m = 0u;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m = bf2_absmax(m, y[i][k]);
+                m &= 0x7FFF7FFFu;
+                m = max(m & 0xFFFFu, m >> 16);
+                m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));  // the block's other half
+                const int e = block_exponent<7>(m);
+                const Bf16Grid gr = bf16_grid_unit(e);
+                const uint32_t scl = bf16_pow2_pair(e);
+                if (e != 125) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) y[i][k] = bf2_mul(bf2_grid(y[i][k], gr) | (y[i][k] & 0x80008000u), scl);
+                } else {  // the upper clamp: saturate at +-6; a NaN or Inf block poisons its outputs
+                    const bool pois = m >= 0x7F80u;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t u = bf2_sat(bf2_grid(y[i][k], gr) | (y[i][k] & 0x80008000u), 0x40C040C0u);
+                        y[i][k] = pois ? 0x7FC07FC0u : bf2_mul(u, scl);
+                    }
+                }
+                uint32_t* d = trow + 8 * i * RW;
+                *reinterpret_cast<uint4*>(d) = make_uint4(y[i][0], y[i][1], y[i][2], y[i][3]);
+                *reinterpret_cast<uint4*>(d + 4) = make_uint4(y[i][4], y[i][5], y[i][6], y[i][7]);
+            }
         }
         __syncwarp();
 
@@ -557,10 +615,10 @@ cudaError_t dispatch(const ColwiseArgs& a, cudaStream_t s) {
     const bool vec = aligned(a.x, 32) && (a.ldx * es) % 32 == 0 && (a.K * es) % 32 == 0;
     const int dst = (aligned(a.data, 32) && a.K % 32 == 0) ? 2 : (aligned(a.data, 16) && a.K % 16 == 0) ? 1 : 0;
     if (!vec) return launch_one<ELT, false, 0>(a, s);
-    if (ELT == Elt::BF16 && a.K % 32 == 0 && aligned(a.data, 16)) {
+    if (a.K % 32 == 0 && aligned(a.data, 16)) {
         const int64_t bands = ceil_div(a.rows, 32), gx = ceil_div(ceil_div(a.K, 64), kTileWarps);
         const unsigned gy = (unsigned)(bands < 65535 ? bands : 65535);
-        tile64_kernel<<<dim3((unsigned)gx, gy), 32 * kTileWarps, 0, s>>>(a, bands);
+        tile64_kernel<ELT><<<dim3((unsigned)gx, gy), 32 * kTileWarps, 0, s>>>(a, bands);
         return cudaGetLastError();
     }
     if (dst == 2) return launch_one<ELT, true, 2>(a, s);

@@ -155,22 +155,34 @@ def test_edge_shapes(mx, shape, dt):
 
 
 @pytest.mark.parametrize("shape", [(1, 32), (32, 64), (33, 96), (100, 160), (257, 320), (70, 4096)])
-def test_columnwise_tile_path_bf16(mx, shape):
-    """bf16 with K % 32 == 0: the 32x64 warp-tile columnwise path.  Odd and
-    half-filled column tiles, ragged bands, row and column exponent spreads
-    of 2^+-40 (so 32x1 payloads fall into E4M3 subnormals), blocks at the
-    upper clamp, and NaN / Inf / zero blocks."""
+@pytest.mark.parametrize("dt", ["bf16", "fp32"])
+def test_columnwise_tile_path(mx, shape, dt):
+    """K % 32 == 0: the 32x64 warp-tile columnwise path (fp32 through the
+    E2M1 conversion).  Odd and half-filled column tiles, ragged bands, row
+    and column exponent spreads of 2^+-40 (so 32x1 payloads fall into E4M3
+    subnormals), blocks at the upper clamp, and NaN / Inf / zero blocks."""
     rows, K = shape
     g = np.random.default_rng(zlib.crc32(repr(("tile64", shape)).encode()))
     w = g.standard_normal(shape) * np.ldexp(1.0, g.integers(-40, 40, size=(rows, 1)))
     w *= np.ldexp(1.0, g.integers(-8, 8, size=(1, K)))
-    x = syn.f32_to_bf16_bits(w.astype(np.float32))
-    if rows > 2:
-        x[1, :] = np.where(np.arange(K) % 3 == 0, 0x7F7F, 0xFF70)  # near 6 * 2^125: the upper clamp
-        x[2, :32] = 0
-    if rows > 40 and K > 40:
-        x[37, 5] = 0x7FC0   # NaN block
-        x[40, 33] = 0xFF80  # -Inf block
+    w = w.astype(np.float32)
+    if dt == "bf16":
+        x = syn.f32_to_bf16_bits(w)
+        if rows > 2:
+            x[1, :] = np.where(np.arange(K) % 3 == 0, 0x7F7F, 0xFF70)  # near 6 * 2^125: the upper clamp
+            x[2, :32] = 0
+        if rows > 40 and K > 40:
+            x[37, 5] = 0x7FC0   # NaN block
+            x[40, 33] = 0xFF80  # -Inf block
+    else:
+        x = w
+        u = x.view(np.uint32)
+        if rows > 2:
+            u[1, :] = np.where(np.arange(K) % 3 == 0, 0x7F7FFFFF, 0xFF6FFFFF)  # near the fp32 maximum: the clamp
+            x[2, :32] = 0.0
+        if rows > 40 and K > 40:
+            u[37, 5] = 0x7FC00001   # NaN block
+            u[40, 33] = 0xFF800000  # -Inf block
     run_all_and_compare(mx, x)
 
 
