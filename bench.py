@@ -458,13 +458,14 @@ def run_fp32(args, lib, dev, stream, world):
     return out
 
 
-def run_e2e(args, lib, dev, x_host, world, chunks: int = 8):
+def run_e2e(args, lib, dev, x_host, world, chunks: int = 2):
     """The same five conversions through the public API with the weight in
     pinned host memory and every result copied back to pinned host memory.
     The weight is cut into row chunks (multiples of 128 rows, so every
     scale layout splits into contiguous slices); chunk c's upload, its five
     conversions and its downloads run on three streams, so copies overlap
-    the kernels of neighbouring chunks."""
+    the kernels and copies of the other chunk.  Two chunks measured best:
+    each chunk adds eight copies, and 4 / 8 / 16 chunks were slower."""
     import torch
 
     rows_c = ROWS // chunks
