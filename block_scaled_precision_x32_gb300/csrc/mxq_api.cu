@@ -3,6 +3,8 @@
 // in include/mxq.h.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include <cstdint>
 
 #include "../../include/mxq.h"
@@ -11,14 +13,14 @@
 namespace mxq {
 
 int sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];  // zero-initialised; one SM count per device, written once
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
     const int slot = dev < 64 ? dev : 63;
-    if (cached[slot] == 0) {
+    if (cached[slot].load(std::memory_order_relaxed) == 0) {
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-        cached[slot] = n;
+        cached[slot].store(n, std::memory_order_relaxed);
     }
     return cached[slot];
 }

@@ -364,11 +364,12 @@ cudaError_t launch_one(const Block128Args& a, cudaStream_t s) {
     const int64_t tr = ceil_div(a.rows, 128), tc = ceil_div(a.K, 128);
     if (tc > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const unsigned gy = (unsigned)(tr < 65535 ? tr : 65535);
-    static bool configured = false;
-    if (!configured) {  // no shared memory to speak of: give L1 the whole carveout
-        cudaFuncSetAttribute(block128_kernel<ELT, VEC, DST>, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
-        configured = true;
-    }
+    // no shared memory to speak of: give L1 the whole carveout (a hint, set once)
+    static const bool configured = [] {
+        return cudaFuncSetAttribute(block128_kernel<ELT, VEC, DST>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    0) == cudaSuccess;
+    }();
+    (void)configured;
     block128_kernel<ELT, VEC, DST><<<dim3((unsigned)tc, gy), T128<ELT>::NT, 0, s>>>(a, tr, tc);
     return cudaGetLastError();
 }

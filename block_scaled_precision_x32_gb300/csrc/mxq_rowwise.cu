@@ -313,13 +313,15 @@ template <RowMode MODE, Elt ELT, bool VEC, int DST>
 cudaError_t launch_one(const RowwiseArgs& a, cudaStream_t s) {
     const int64_t nb = (a.K + 31) / 32;
     const int64_t total = a.rows * nb;
-    static int occ = 0;
-    if (occ == 0) {
-        cudaError_t err =
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rowwise_kernel<MODE, ELT, VEC, DST>, kThreads, 0);
-        if (err != cudaSuccess) return err;
-        if (occ < 1) occ = 1;
-    }
+    // resident CTAs per SM, asked once (thread-safe static initialisation)
+    static const int occ = [] {
+        int o = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, rowwise_kernel<MODE, ELT, VEC, DST>, kThreads, 0) !=
+                cudaSuccess ||
+            o < 1)
+            o = 1;
+        return o;
+    }();
     // Grid size, measured on 8192 x 8192 (a sweep of 1..12 x the resident grid
     // and one thread per block): the projection, whose traffic is half writes,
     // and every fp32 form (128 bytes per thread) are fastest with a thread per
