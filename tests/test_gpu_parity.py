@@ -718,6 +718,49 @@ def test_packed_mxfp4_moe_expert_sampled(mx):
 
 # ------------------------------------------------------- fast-math build
 
+def test_concurrent_host_threads(mx):
+    """Four host threads, each on its own CUDA stream, converting different
+    weights at once through the C ABI (ctypes drops the GIL around the
+    calls): the bytes equal those of one-thread runs."""
+    import threading
+
+    xs = [dev_bf16(syn.normal_bf16(512, 1024 + 32 * i, seed=70 + i)) for i in range(4)]
+    want = []
+    for x in xs:
+        d, s = mx.mxfp8_row_direct(x, "swizzled")
+        bd, bs = mx.fp8_block128_direct(x)
+        cd, cs = mx.mxfp8_col_direct(x, "compact")
+        want.append([host_bits(t) for t in (mx.fake_quant_mxfp4(x), d, s, bd, bs, cd, cs)])
+    torch.cuda.synchronize()
+    got = [None] * 4
+    errors = []
+
+    def work(i):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(20):
+                    x = xs[i]
+                    y = mx.fake_quant_mxfp4(x)
+                    d, s = mx.mxfp8_row_direct(x, "swizzled")
+                    bd, bs = mx.fp8_block128_direct(x)
+                    cd, cs = mx.mxfp8_col_direct(x, "compact")
+                st.synchronize()
+                got[i] = [host_bits(t) for t in (y, d, s, bd, bs, cd, cs)]
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for i in range(4):
+        for a, b in zip(got[i], want[i]):
+            np.testing.assert_array_equal(a, b)
+
+
 def test_fast_math_build_gives_identical_bytes(mx):
     """The same sources built with --use_fast_math give identical bytes
     (TE PR #3264, "Test results (B200)")."""
