@@ -623,12 +623,16 @@ def test_quantize_export_one_call(mx):
 
 # ------------------------------------------------------ skip-update flag
 
-def test_skip_flag_leaves_every_output_untouched(mx):
+@pytest.mark.parametrize("dt", ["bf16", "fp32"])
+def test_skip_flag_leaves_every_output_untouched(mx, dt):
     """A nonzero device flag makes the *_update converters write nothing --
-    payloads, scales (padding included) and tile scales keep their bytes."""
+    payloads, scales (padding included) and tile scales keep their bytes
+    (fp32: the pipelined blockwise kernel included)."""
     x = dev_bf16(syn.normal_bf16(256, 512, seed=31))
+    if dt == "fp32":
+        x = x.float()
     skip = torch.ones(1, dtype=torch.int32, device="cuda")
-    y = torch.full((256, 512), 1.0, dtype=torch.bfloat16, device="cuda")
+    y = torch.full((256, 512), 1.0, dtype=x.dtype, device="cuda")
     d = torch.full((256, 512), 0x5A, dtype=torch.uint8, device="cuda")
     s = torch.full((mx.scale_bytes(256, 512, "swizzled"),), 0x5A, dtype=torch.uint8, device="cuda")
     bd = torch.full((256, 512), 0x5A, dtype=torch.uint8, device="cuda")
@@ -647,7 +651,8 @@ def test_skip_flag_leaves_every_output_untouched(mx):
     rd, rs = mx.mxfp8_row_direct(x, "swizzled")
     rbd, rbs = mx.fp8_block128_direct(x)
     torch.cuda.synchronize()
-    assert torch.equal(y.view(torch.int16), ry.view(torch.int16))
+    assert torch.equal(y.view(torch.int16 if dt == "bf16" else torch.int32),
+                       ry.view(torch.int16 if dt == "bf16" else torch.int32))
     assert torch.equal(d, rd) and torch.equal(s, rs.reshape(-1))
     assert torch.equal(bd, rbd) and torch.equal(bs.view(torch.int32), rbs.reshape(-1).view(torch.int32))
 
