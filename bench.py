@@ -621,6 +621,48 @@ def cpu_baseline_all_cores(budget_s: float = 10.0):
                       f"whole step (5 conversions) each, the single-threaded C oracle unchanged, {wall:.1f} s wall"}
 
 
+def _oracle_moe_slab(task):
+    """The first `rows` rows of MoE expert `expert` (7184 bf16 columns)
+    through the oracle: MXFP8 rowwise into swizzled scales, then the export
+    to compact.  Returns (seconds, bytes by the GPU section's definitions of
+    both conversions)."""
+    import oracle
+    from block_scaled_precision_x32_gb300 import synthetic as syn
+
+    expert, rows = task
+    x = syn.moe_expert_bf16(expert, rows=rows)  # row-major draws: the expert's first rows
+    K = x.shape[1]
+    t = time.perf_counter()
+    _, s = oracle.mxfp8_row_direct(x, oracle.SWIZZLED)
+    oracle.export_scales(s, oracle.SWIZZLED, rows, K)
+    dt = time.perf_counter() - t
+    return dt, 3 * rows * K + 2 * s.size + rows * (-(-K // 32))
+
+
+def cpu_baseline_moe(rows: int = 512):
+    """The MoE-stack conversions (rowwise into swizzled scales, then export)
+    on the oracle, on bounded samples: a `rows`-row slab of one expert on one
+    core, and one such slab of a different expert per host core at once."""
+    import multiprocessing as mp
+
+    from block_scaled_precision_x32_gb300 import synthetic as syn
+
+    dt1, b1 = _oracle_moe_slab((0, rows))
+    n = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(n) as pool:
+        pool.map(_oracle_slab, [(128, 6000 + i) for i in range(n)])  # start every worker, load the oracle
+        t = time.perf_counter()
+        res = pool.map(_oracle_moe_slab, [(e % syn.MOE_EXPERTS, rows) for e in range(n)], chunksize=1)
+        wall = time.perf_counter() - t
+    nbytes = sum(b for _, b in res)
+    return {"one_core": {"value": round(b1 / dt1 / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "seconds": round(dt1, 2)},
+            "all_cores": {"value": round(nbytes / wall / 1e9, 5), "unit": "GB/s", "cores": n, "kind": "oracle",
+                          "seconds": round(wall, 2)},
+            "sample": f"{rows}-row slabs of the {syn.MOE_ROWS} x {syn.MOE_K} bf16 experts (one slab per process), "
+                      f"MXFP8 rowwise into swizzled scales + export, the single-threaded C oracle unchanged"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -705,6 +747,8 @@ def main(argv=None):
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline()
             res["cpu_baseline_all_cores"] = cpu_baseline_all_cores()
+            if not args.no_moe:
+                res["cpu_baseline_moe"] = cpu_baseline_moe()
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
