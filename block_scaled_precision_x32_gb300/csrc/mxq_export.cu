@@ -137,7 +137,8 @@ constexpr int kFlatThreads = 256;
 
 template <int VW>
 __global__ void __launch_bounds__(kFlatThreads) unswizzle_flat_kernel(ExportArgs a, int64_t tiles_r) {
-    constexpr int NW = kFlatThreads / 32;  // warps; a multiple of 8
+    constexpr int NW = kFlatThreads / 32;  // warps
+    static_assert(NW % 8 == 0, "the group walk below steps by NW / 8 slot words: NW must be a multiple of 8");
     // nb table entries, then ct + 1 staged tiles of kTileWords words (the
     // spare tile lets a word read column tile j/4 + 1 unconditionally; what
     // it holds is shifted or masked away)
