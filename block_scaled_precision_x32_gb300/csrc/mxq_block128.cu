@@ -7,15 +7,13 @@
 //
 // One CTA per tile; the tile is read from HBM once.  A tile is 512 blocks of
 // 1x32; each lane owns whole blocks (2 per lane for bf16 with 256 threads, 1
-// for fp32 with 512), read as 32-byte vectors.  Pass 1 reads the blocks
-// (asking L1 to keep the lines) and keeps only their exponents; the tile
-// maximum is one warp redux plus a pass through shared memory; pass 2
-// re-reads the blocks -- from L1, the bf16 tile being 32 KB -- encodes
-// them and writes 32 payload bytes per block.  Holding no tile data across
-// the barrier keeps registers low and lets more tiles stream per SM.  An
-// fp32 tile (64 KB, one block per lane) leaves too little L1 for pass 2,
-// so there each lane keeps its block in registers across the barrier
-// (8192 x 8192: 68 us against 81 us re-reading).
+// for fp32 with 512), read as 32-byte vectors and kept in registers (32 per
+// lane): pass 1 takes the block exponents, the tile maximum is one warp
+// redux plus a pass through shared memory, and pass 2 encodes the held
+// blocks and writes 32 payload bytes per block.  (Re-reading the tile from
+// L1 in pass 2 instead, with no tile data across the barrier, measured
+// 33.6 us for bf16 and 81 us for fp32 on 8192 x 8192, against 31.8 and
+// 68 us holding.)  fp32 with aligned rows runs block128_pipe_kernel below.
 #include <cuda_runtime.h>
 
 #include "mxq_device.cuh"
@@ -38,19 +36,14 @@ struct T128<Elt::FP32> {
 };
 
 // One block of the tile as SEGS x 8 words (missing elements read as +0).
-// PASS 1 reads from HBM and asks L1 to keep the lines; PASS 2 reads them
-// again (an L1 hit in the common case) and lets them go.
-template <Elt ELT, bool VEC, int PASS>
+template <Elt ELT, bool VEC>
 __device__ __forceinline__ void load_blk(uint32_t (&v)[T128<ELT>::SEGS][8], const char* p, int valid) {
     using P = T128<ELT>;
 #pragma unroll
     for (int s = 0; s < P::SEGS; ++s) {
         if constexpr (VEC) {
             if (s * P::SEG_ELEMS < valid) {
-                if constexpr (PASS == 1)
-                    ld32_keep(v[s], p + 32 * s);
-                else
-                    ld32_drop(v[s], p + 32 * s);
+                ld32(v[s], p + 32 * s);
             } else {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) v[s][k] = 0u;
@@ -197,31 +190,25 @@ __global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB)
     if (a.skip != nullptr && *a.skip != 0) return;  // skip-update request: write nothing
 
     for (int64_t ti = blockIdx.y; ti < tiles_r; ti += gridDim.y) {
-        const char* xp[P::BPL];
         int valid[P::BPL];
         int eb[P::BPL];
         bool pois[P::BPL];
         int local = kNoBlock;
-        // fp32 (one block per lane): the block stays in registers for pass 2
-        constexpr bool kHold = ELT == Elt::FP32;
-        uint32_t held[kHold ? P::SEGS : 1][8];
+        uint32_t held[P::BPL][P::SEGS][8];  // the lane's blocks, kept for pass 2
         // pass 1: block exponents
 #pragma unroll
         for (int i = 0; i < P::BPL; ++i) {
             const int q = i * P::NT + t;  // block of the tile: row q/4, column block q%4
             const int64_t row = ti * 128 + (q >> 2), col0 = tj * 128 + (q & 3) * 32;
             valid[i] = row < a.rows ? (int)max((int64_t)0, min((int64_t)32, a.K - col0)) : 0;
-            xp[i] = static_cast<const char*>(a.x) + (row * a.ldx + col0) * P::ES;
             uint32_t v[P::SEGS][8];
-            load_blk<ELT, VEC, 1>(v, xp[i], valid[i]);
+            load_blk<ELT, VEC>(v, static_cast<const char*>(a.x) + (row * a.ldx + col0) * P::ES, valid[i]);
             eb[i] = block_exp<ELT>(v, pois[i]);
             if (!pois[i] && valid[i] > 0) local = max(local, eb[i]);
-            if constexpr (kHold) {
 #pragma unroll
-                for (int s2 = 0; s2 < P::SEGS; ++s2)
+            for (int s2 = 0; s2 < P::SEGS; ++s2)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) held[s2][k] = v[s2][k];
-            }
+                for (int k = 0; k < 8; ++k) held[i][s2][k] = v[s2][k];
         }
         local = __reduce_max_sync(0xffffffffu, local);
         if ((t & 31) == 0) warp_max[t >> 5] = local;
@@ -239,14 +226,10 @@ __global__ void __launch_bounds__(T128<ELT>::NT, T128<ELT>::MINB)
         for (int i = 0; i < P::BPL; ++i) {
             if (valid[i] <= 0) continue;
             uint32_t v[P::SEGS][8];
-            if constexpr (kHold) {
 #pragma unroll
-                for (int s2 = 0; s2 < P::SEGS; ++s2)
+            for (int s2 = 0; s2 < P::SEGS; ++s2)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) v[s2][k] = held[s2][k];
-            } else {
-                load_blk<ELT, VEC, 2>(v, xp[i], valid[i]);
-            }
+                for (int k = 0; k < 8; ++k) v[s2][k] = held[i][s2][k];
             const int q = i * P::NT + t;
             encode_block<ELT, DST>(v, eb[i], T, pois[i], valid[i],
                                    a.data + (ti * 128 + (q >> 2)) * a.K + tj * 128 + (q & 3) * 32);
@@ -364,12 +347,6 @@ cudaError_t launch_one(const Block128Args& a, cudaStream_t s) {
     const int64_t tr = ceil_div(a.rows, 128), tc = ceil_div(a.K, 128);
     if (tc > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const unsigned gy = (unsigned)(tr < 65535 ? tr : 65535);
-    // no shared memory to speak of: give L1 the whole carveout (a hint, set once)
-    static const bool configured = [] {
-        return cudaFuncSetAttribute(block128_kernel<ELT, VEC, DST>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                    0) == cudaSuccess;
-    }();
-    (void)configured;
     block128_kernel<ELT, VEC, DST><<<dim3((unsigned)tc, gy), T128<ELT>::NT, 0, s>>>(a, tr, tc);
     return cudaGetLastError();
 }

@@ -101,18 +101,6 @@ __device__ __forceinline__ void ld32(uint32_t (&w)[8], const void* p) {
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
                  : "l"(p));
 }
-// 32-byte loads with an L1 eviction hint: "keep" for a first read whose
-// lines are read again soon, "drop" for that second, last read.
-__device__ __forceinline__ void ld32_keep(uint32_t (&w)[8], const void* p) {
-    asm volatile("ld.global.L1::evict_last.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                 : "l"(p));
-}
-__device__ __forceinline__ void ld32_drop(uint32_t (&w)[8], const void* p) {
-    asm volatile("ld.global.L1::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                 : "l"(p));
-}
 __device__ __forceinline__ void st32(void* p, const uint32_t (&w)[8]) {
     asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
                  "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
