@@ -141,6 +141,21 @@ def _need_cuda(*ts):
             raise ValueError("libmxq works on CUDA tensors only")
 
 
+def _check_bytes(t: torch.Tensor, need: int, name: str, what: str):
+    """The C ABI sees only a pointer: a buffer shorter than the layout would
+    be read (or written) past its end, so the binding checks it here."""
+    if t.dtype != torch.uint8 or not t.is_contiguous() or t.numel() < need:
+        raise ValueError(f"{name} must be a contiguous uint8 buffer of at least {what} = {need} bytes")
+
+
+def _check_storage(lib, data, scales, rows: int, K: int, layout):
+    """Sizes of an MXFP8 storage handed to an export: rows*K payload bytes
+    and the scale bytes of its layout."""
+    _check_bytes(scales, lib.scale_bytes(rows, K, _LAYOUTS[layout]), "scales", "mxq_scale_bytes(rows, K, layout)")
+    if data is not None and (not data.is_contiguous() or data.numel() != rows * K or data.element_size() != 1):
+        raise ValueError("data must be the contiguous rows*K payload bytes of the storage")
+
+
 class Library:
     """One loaded libmxq variant (``fastmath=True`` loads the --use_fast_math build)."""
 
@@ -162,6 +177,8 @@ class Library:
         L.mxq_fp8_block128_direct_update.argtypes = [vp, ci, i64, i64, i64, vp, vp, vp, vp]
         L.mxq_mxfp4_pack.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp]
         L.mxq_mxfp8_col_direct.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp]
+        L.mxq_mxfp4_pack_update.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp, vp]
+        L.mxq_mxfp8_col_direct_update.argtypes = [vp, ci, i64, i64, i64, vp, vp, ci, vp, vp]
         L.mxq_export_mxfp8_grouped.argtypes = [ctypes.POINTER(_Storage), i64, vp, ctypes.c_size_t,
                                                ctypes.POINTER(_Components), vp]
         L.mxq_quantize_export_mxfp8.argtypes = [vp, ci, i64, i64, i64, vp, vp, ctypes.POINTER(_Components), vp]
@@ -176,7 +193,8 @@ class Library:
         for fn in ("mxq_fake_quant_mxfp4", "mxq_mxfp8_row_direct", "mxq_fp8_block128_direct", "mxq_dequantize",
                    "mxq_export_mxfp8", "mxq_fake_quant_mxfp4_update", "mxq_mxfp8_row_direct_update",
                    "mxq_fp8_block128_direct_update", "mxq_mxfp4_pack", "mxq_mxfp8_col_direct",
-                   "mxq_export_mxfp8_grouped", "mxq_quantize_export_mxfp8"):
+                   "mxq_mxfp4_pack_update", "mxq_mxfp8_col_direct_update", "mxq_export_mxfp8_grouped",
+                   "mxq_quantize_export_mxfp8"):
             getattr(L, fn).restype = ci
         self.L = L
 
@@ -232,14 +250,16 @@ class Library:
                               skip: Optional[torch.Tensor] = None) -> "Call":
         return self._plan_rowwise_quant("mxq_mxfp8_row_direct", x, layout, data, scales, lambda r, k: r * k, skip)
 
-    def plan_mxfp4_pack(self, x: torch.Tensor, layout, packed: torch.Tensor, scales: torch.Tensor) -> "Call":
+    def plan_mxfp4_pack(self, x: torch.Tensor, layout, packed: torch.Tensor, scales: torch.Tensor,
+                        skip: Optional[torch.Tensor] = None) -> "Call":
         return self._plan_rowwise_quant("mxq_mxfp4_pack", x, layout, packed, scales, lambda r, k: r * ((k + 1) // 2),
-                                        None)
+                                        skip)
 
-    def plan_mxfp8_col_direct(self, x: torch.Tensor, layout, data: torch.Tensor, scales: torch.Tensor) -> "Call":
+    def plan_mxfp8_col_direct(self, x: torch.Tensor, layout, data: torch.Tensor, scales: torch.Tensor,
+                              skip: Optional[torch.Tensor] = None) -> "Call":
         """Columnwise MXFP8: data [rows, K]; scales hold the K x ceil(rows/32)
         scale matrix of the transposed tensor in ``layout``."""
-        _need_cuda(x, data, scales)
+        _need_cuda(x, data, scales, skip)
         dt = _dt_code(x)
         lay = _LAYOUTS[layout]
         rows, K, ldx = _rows_view(x)
@@ -248,8 +268,12 @@ class Library:
         if not scales.is_contiguous() or scales.dtype != torch.uint8 or scales.numel() < self.scale_bytes(K, rows, lay):
             raise ValueError("scales must be a contiguous uint8 buffer of mxq_scale_bytes(K, rows) bytes")
         args = (ctypes.c_void_p(x.data_ptr()), dt, rows, K, ldx, ctypes.c_void_p(data.data_ptr()),
-                ctypes.c_void_p(scales.data_ptr()), lay, _stream(x))
-        return Call(self, self.L.mxq_mxfp8_col_direct, args, "mxq_mxfp8_col_direct", (x, data, scales), x.device)
+                ctypes.c_void_p(scales.data_ptr()), lay)
+        if skip is not None:
+            return Call(self, self.L.mxq_mxfp8_col_direct_update, args + (_skip_ptr(skip), _stream(x)),
+                        "mxq_mxfp8_col_direct_update", (x, data, scales, skip), x.device)
+        return Call(self, self.L.mxq_mxfp8_col_direct, args + (_stream(x),), "mxq_mxfp8_col_direct",
+                    (x, data, scales), x.device)
 
     def plan_fp8_block128_direct(self, x: torch.Tensor, data: torch.Tensor, tile_scale_inv: torch.Tensor,
                                  skip: Optional[torch.Tensor] = None) -> "Call":
@@ -291,12 +315,25 @@ class Library:
                 raise ValueError("out must have data's shape")
             K = data.shape[-1] if data.dim() else 1
             rows = data.numel() // K if K else 0
+        if data.dtype not in (torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2):
+            raise ValueError("data must hold payload bytes (uint8 or an fp8 view)")
+        lay = _LAYOUTS[layout]
+        if scales is not None:
+            # the kernels read every scale of the layout: a short buffer would be read past its end
+            need = self.scale_bytes(K, rows, lay) if columnwise else self.scale_bytes(rows, K, lay)
+            _check_bytes(scales, need, "scales", "mxq_scale_bytes(K, rows, layout)" if columnwise
+                         else "mxq_scale_bytes(rows, K, layout)")
+        else:
+            if (not tile_scale_inv.is_contiguous() or tile_scale_inv.dtype != torch.float32
+                    or tile_scale_inv.numel() < self.tile_scale_count(rows, K)):
+                raise ValueError("tile_scale_inv must be a contiguous fp32 tensor of "
+                                 "ceil(rows/128)*ceil(K/128) values")
         q = _Quantized()
         q.kind = _MXFP4 if mxfp4 else (_MXFP8_COL if columnwise else (_MXFP8_ROW if scales is not None else _BLOCK128))
         q.data = data.data_ptr()
         q.rows, q.K = rows, K
         q.fp8 = _fp8_code(fp8)
-        q.lay = _LAYOUTS[layout]
+        q.lay = lay
         q.scales = scales.data_ptr() if scales is not None else None
         q.tile_scale_inv = tile_scale_inv.data_ptr() if tile_scale_inv is not None else None
         odt = _FP16 if out.dtype == torch.float16 else _dt_code(out)
@@ -316,6 +353,9 @@ class Library:
             rows *= d
         nb = scale_cols(K)
         _need_cuda(scales, data, scale_out)
+        _check_storage(self, data, scales, rows, K, layout)
+        if scale_out is not None and (scale_out.dtype != torch.uint8 or not scale_out.is_contiguous()):
+            raise ValueError("scale_out must be a contiguous uint8 tensor")
         st = _Storage()
         st.data = data.data_ptr() if data is not None else None
         st.scales = scales.data_ptr()
@@ -370,7 +410,7 @@ class Library:
         return data, tile_scale_inv
 
     def mxfp8_col_direct(self, x: torch.Tensor, layout="compact", data: Optional[torch.Tensor] = None,
-                         scales: Optional[torch.Tensor] = None):
+                         scales: Optional[torch.Tensor] = None, skip: Optional[torch.Tensor] = None):
         """Returns (payload uint8 [rows, K], scales of the K x ceil(rows/32)
         transposed scale matrix: compact (K, nbr), padded/swizzled (Kp, Cp))."""
         rows, K, _ = _rows_view(x)
@@ -382,11 +422,11 @@ class Library:
                 scales = torch.empty((K, nbr), dtype=torch.uint8, device=x.device)
             else:
                 scales = torch.empty(((K + 127) // 128 * 128, (nbr + 3) // 4 * 4), dtype=torch.uint8, device=x.device)
-        self.plan_mxfp8_col_direct(x, layout, data, scales)()
+        self.plan_mxfp8_col_direct(x, layout, data, scales, skip)()
         return data, scales
 
     def mxfp4_pack(self, x: torch.Tensor, layout="compact", packed: Optional[torch.Tensor] = None,
-                   scales: Optional[torch.Tensor] = None):
+                   scales: Optional[torch.Tensor] = None, skip: Optional[torch.Tensor] = None):
         """Returns (nibbles uint8 (*shape[:-1], ceil(K/2)), scales) of the
         packed MXFP4 form; scales shaped as in mxfp8_row_direct."""
         rows, K, _ = _rows_view(x)
@@ -394,7 +434,7 @@ class Library:
             packed = torch.empty(tuple(x.shape[:-1]) + ((K + 1) // 2,), dtype=torch.uint8, device=x.device)
         if scales is None:
             scales = self._scale_buffer(x, rows, K, layout)
-        self.plan_mxfp4_pack(x, layout, packed, scales)()
+        self.plan_mxfp4_pack(x, layout, packed, scales, skip)()
         return packed, scales
 
     def _scale_buffer(self, x, rows, K, layout):
@@ -443,7 +483,12 @@ class Library:
                 rows *= v
             data, scales = d.get("data"), d["scales"]
             _need_cuda(data, scales)
-            dev = scales.device
+            _check_storage(self, data, scales, rows, K, d.get("layout", "compact"))
+            for t in (data, scales):
+                if t is not None and dev is not None and t.device != dev:
+                    raise ValueError("every storage of a grouped export must sit on one device")
+                if t is not None:
+                    dev = t.device
             st[g].data = data.data_ptr() if data is not None else None
             st[g].scales = scales.data_ptr()
             st[g].fp8 = _fp8_code(d.get("fp8", "e4m3"))
@@ -454,6 +499,12 @@ class Library:
             sizes.append((shape, rows, nb, view))
             keep.append((data, scales))
         need = sum(rows * nb for _, rows, nb, view in sizes if not view)
+        if scale_out is not None:
+            _need_cuda(scale_out)
+            if dev is not None and scale_out.device != dev:
+                raise ValueError("scale_out must sit on the storages' device")
+            if scale_out.dtype != torch.uint8 or not scale_out.is_contiguous():
+                raise ValueError("scale_out must be a contiguous uint8 tensor")
         if scale_out is None and need:
             scale_out = torch.empty(need, dtype=torch.uint8, device=dev)
         comps = (_Components * max(n, 1))()
@@ -543,12 +594,12 @@ def mxq_fp8_block128_direct(x, data=None, tile_scale_inv=None, skip=None):
     return library().fp8_block128_direct(x, data, tile_scale_inv, skip)
 
 
-def mxq_mxfp8_col_direct(x, layout="compact", data=None, scales=None):
-    return library().mxfp8_col_direct(x, layout, data, scales)
+def mxq_mxfp8_col_direct(x, layout="compact", data=None, scales=None, skip=None):
+    return library().mxfp8_col_direct(x, layout, data, scales, skip)
 
 
-def mxq_mxfp4_pack(x, layout="compact", packed=None, scales=None):
-    return library().mxfp4_pack(x, layout, packed, scales)
+def mxq_mxfp4_pack(x, layout="compact", packed=None, scales=None, skip=None):
+    return library().mxfp4_pack(x, layout, packed, scales, skip)
 
 
 def mxq_dequantize(data, **kw):

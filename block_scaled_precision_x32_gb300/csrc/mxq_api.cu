@@ -129,18 +129,25 @@ mxq_status mxq_mxfp8_row_direct(const void* x, mxq_dtype dt, int64_t rows, int64
     return rowwise_quant(mxq::RowMode::MXFP8, x, dt, rows, K, ldx, data, scales, lay, nullptr, stream);
 }
 
+mxq_status mxq_mxfp4_pack_update(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* packed,
+                                 uint8_t* scales, mxq_scale_layout lay, const int32_t* skip, cudaStream_t stream) {
+    return rowwise_quant(mxq::RowMode::MXFP4, x, dt, rows, K, ldx, packed, scales, lay, skip, stream);
+}
+
 mxq_status mxq_mxfp4_pack(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* packed,
                           uint8_t* scales, mxq_scale_layout lay, cudaStream_t stream) {
     return rowwise_quant(mxq::RowMode::MXFP4, x, dt, rows, K, ldx, packed, scales, lay, nullptr, stream);
 }
 
-mxq_status mxq_mxfp8_col_direct(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* data,
-                                uint8_t* scales, mxq_scale_layout lay, cudaStream_t stream) {
+mxq_status mxq_mxfp8_col_direct_update(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                       uint8_t* data, uint8_t* scales, mxq_scale_layout lay, const int32_t* skip,
+                                       cudaStream_t stream) {
     mxq_status st = check_dtype(dt);
     if (st != MXQ_OK) return st;
     if (!valid_shape(rows, K, ldx) || !valid_layout(lay)) return MXQ_ERR_INVALID_ARG;
     if (rows == 0 || K == 0) return MXQ_OK;
     if (!x || !data || !scales || !aligned(x, elt_size(dt))) return MXQ_ERR_INVALID_ARG;
+    if (skip && !aligned(skip, 4)) return MXQ_ERR_INVALID_ARG;
     mxq::ColwiseArgs a{};
     a.x = x;
     a.data = data;
@@ -149,7 +156,13 @@ mxq_status mxq_mxfp8_col_direct(const void* x, mxq_dtype dt, int64_t rows, int64
     a.K = K;
     a.ldx = ldx;
     a.lay = (int)lay;
+    a.skip = skip;
     return launch_status(mxq::launch_colwise(elt_of(dt), a, stream));
+}
+
+mxq_status mxq_mxfp8_col_direct(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx, uint8_t* data,
+                                uint8_t* scales, mxq_scale_layout lay, cudaStream_t stream) {
+    return mxq_mxfp8_col_direct_update(x, dt, rows, K, ldx, data, scales, lay, nullptr, stream);
 }
 
 mxq_status mxq_fp8_block128_direct_update(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,

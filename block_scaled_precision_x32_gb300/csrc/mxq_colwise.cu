@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(ColwiseArgs a, int64_
     const int64_t jb = (int64_t)blockIdx.x * kWarps + w;  // 1x32 block column of this warp
     const int64_t col0 = jb * 32;
     uint32_t* my = tile[w] + t * P::ROW_WORDS;
+    if (a.skip != nullptr && *a.skip != 0) return;  // skip-update request: write nothing
 
     for (int64_t band = blockIdx.y; band < bands; band += gridDim.y) {
         const int64_t r = band * 32 + t;
@@ -327,6 +328,7 @@ __global__ void __launch_bounds__(32 * kTileWarps, 16) tile64_kernel(ColwiseArgs
     const bool cvalid = col0 + 16 * q < a.K;                             // this lane's chunk is in the tensor
     const int64_t c0 = col0 + 2 * t;                                     // the column pair this lane scans
     uint32_t* trow = tile[w] + g * RW + 8 * q;
+    if (a.skip != nullptr && *a.skip != 0) return;  // skip-update request: write nothing
 
     for (int64_t band = blockIdx.y; band < bands; band += gridDim.y) {
         const int64_t rbase = band * 32 + g;  // rows rbase + 8i, i = 0..3

@@ -35,6 +35,7 @@ struct ColwiseArgs {
     uint8_t* scales;  // transposed scale matrix (K x ceil(rows/32)) in `lay`
     int64_t rows, K, ldx;
     int lay;
+    const int32_t* skip;  // optional device flag: nonzero = write nothing
 };
 
 struct DequantArgs {

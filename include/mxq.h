@@ -192,6 +192,17 @@ MXQ_API mxq_status mxq_mxfp8_row_direct_update(const void* x, mxq_dtype dt, int6
 MXQ_API mxq_status mxq_fp8_block128_direct_update(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
                                                   uint8_t* data, float* tile_scale_inv, const int32_t* skip,
                                                   cudaStream_t stream);
+/* The columnwise copy of the same cached weight (the direct workspace holds
+ * rowwise, columnwise and blockwise forms; TE PR #3264, review flowchart:
+ * every part of the workspace refresh is gated by the skip flag) and the
+ * packed MXFP4 deployment form.  A nonzero flag leaves the payload, the
+ * scales and their padding untouched. */
+MXQ_API mxq_status mxq_mxfp8_col_direct_update(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                               uint8_t* data, uint8_t* scales, mxq_scale_layout lay,
+                                               const int32_t* skip, cudaStream_t stream);
+MXQ_API mxq_status mxq_mxfp4_pack_update(const void* x, mxq_dtype dt, int64_t rows, int64_t K, int64_t ldx,
+                                         uint8_t* packed, uint8_t* scales, mxq_scale_layout lay, const int32_t* skip,
+                                         cudaStream_t stream);
 
 typedef enum {
     MXQ_QUANT_MXFP8_ROW = 0,

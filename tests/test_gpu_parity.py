@@ -626,53 +626,92 @@ def test_quantize_export_one_call(mx):
 @pytest.mark.parametrize("dt", ["bf16", "fp32"])
 def test_skip_flag_leaves_every_output_untouched(mx, dt):
     """A nonzero device flag makes the *_update converters write nothing --
-    payloads, scales (padding included) and tile scales keep their bytes
-    (fp32: the pipelined blockwise kernel included)."""
-    x = dev_bf16(syn.normal_bf16(256, 512, seed=31))
+    payloads, scales (padding included) and tile scales keep their bytes, for
+    every form of the direct workspace: projection, MXFP8 rowwise, MXFP8
+    columnwise (transposed swizzled scales), 128x128 blockwise (fp32: the
+    pipelined kernel included) and packed MXFP4 (TE PR #3264, review: the
+    skip flag gates the whole workspace refresh).  Rows = 200 leave padding
+    in both the row and the transposed scale layouts."""
+    R, K = 200, 512
+    x = dev_bf16(syn.normal_bf16(R, K, seed=31))
     if dt == "fp32":
         x = x.float()
     skip = torch.ones(1, dtype=torch.int32, device="cuda")
-    y = torch.full((256, 512), 1.0, dtype=x.dtype, device="cuda")
-    d = torch.full((256, 512), 0x5A, dtype=torch.uint8, device="cuda")
-    s = torch.full((mx.scale_bytes(256, 512, "swizzled"),), 0x5A, dtype=torch.uint8, device="cuda")
-    bd = torch.full((256, 512), 0x5A, dtype=torch.uint8, device="cuda")
-    bs = torch.full((mx.tile_scale_count(256, 512),), 3.0, dtype=torch.float32, device="cuda")
-    mx.fake_quant_mxfp4(x, out=y, skip=skip)
-    mx.mxfp8_row_direct(x, "swizzled", data=d, scales=s, skip=skip)
-    mx.fp8_block128_direct(x, data=bd, tile_scale_inv=bs, skip=skip)
+
+    def filled(n, v=0x5A):
+        return torch.full((n,), v, dtype=torch.uint8, device="cuda")
+
+    y = torch.full((R, K), 1.0, dtype=x.dtype, device="cuda")
+    d, s = filled(R * K).view(R, K), filled(mx.scale_bytes(R, K, "swizzled"))
+    cd, cs = filled(R * K).view(R, K), filled(mx.scale_bytes(K, R, "swizzled"))
+    pk, ps = filled(R * K // 2).view(R, K // 2), filled(mx.scale_bytes(R, K, "swizzled"))
+    bd = filled(R * K).view(R, K)
+    bs = torch.full((mx.tile_scale_count(R, K),), 3.0, dtype=torch.float32, device="cuda")
+
+    def run_all():
+        mx.fake_quant_mxfp4(x, out=y, skip=skip)
+        mx.mxfp8_row_direct(x, "swizzled", data=d, scales=s, skip=skip)
+        mx.mxfp8_col_direct(x, "swizzled", data=cd, scales=cs, skip=skip)
+        mx.mxfp4_pack(x, "swizzled", packed=pk, scales=ps, skip=skip)
+        mx.fp8_block128_direct(x, data=bd, tile_scale_inv=bs, skip=skip)
+
+    run_all()
     torch.cuda.synchronize()
-    assert bool((y == 1.0).all()) and bool((d == 0x5A).all()) and bool((s == 0x5A).all())
-    assert bool((bd == 0x5A).all()) and bool((bs == 3.0).all())
+    assert bool((y == 1.0).all())
+    for t in (d, s, cd, cs, pk, ps, bd):
+        assert bool((t == 0x5A).all())
+    assert bool((bs == 3.0).all())
     skip.zero_()
-    mx.fake_quant_mxfp4(x, out=y, skip=skip)
-    mx.mxfp8_row_direct(x, "swizzled", data=d, scales=s, skip=skip)
-    mx.fp8_block128_direct(x, data=bd, tile_scale_inv=bs, skip=skip)
+    run_all()
     ry = mx.fake_quant_mxfp4(x)
     rd, rs = mx.mxfp8_row_direct(x, "swizzled")
+    rcd, rcs = mx.mxfp8_col_direct(x, "swizzled")
+    rpk, rps = mx.mxfp4_pack(x, "swizzled")
     rbd, rbs = mx.fp8_block128_direct(x)
     torch.cuda.synchronize()
-    assert torch.equal(y.view(torch.int16 if dt == "bf16" else torch.int32),
-                       ry.view(torch.int16 if dt == "bf16" else torch.int32))
+    iv = torch.int16 if dt == "bf16" else torch.int32
+    assert torch.equal(y.view(iv), ry.view(iv))
     assert torch.equal(d, rd) and torch.equal(s, rs.reshape(-1))
+    assert torch.equal(cd, rcd) and torch.equal(cs, rcs.reshape(-1))
+    assert torch.equal(pk, rpk) and torch.equal(ps, rps.reshape(-1))
     assert torch.equal(bd, rbd) and torch.equal(bs.view(torch.int32), rbs.reshape(-1).view(torch.int32))
+    # and the refreshed bytes are the oracle's (padding of both scale layouts zero)
+    x_np = syn.normal_bf16(R, K, seed=31)
+    if dt == "fp32":
+        x_np = syn.bf16_bits_to_f32(x_np)
+    ocd, ocs = oracle.mxfp8_col_direct(x_np, oracle.SWIZZLED)
+    opk, ops = oracle.mxfp4_pack(x_np, oracle.SWIZZLED)
+    np.testing.assert_array_equal(host_bits(cd), ocd)
+    np.testing.assert_array_equal(host_bits(cs), ocs)
+    np.testing.assert_array_equal(host_bits(pk), opk)
+    np.testing.assert_array_equal(host_bits(ps), ops)
 
 
 def test_skip_flag_in_a_captured_graph(mx):
     """The flag is read at replay: a graph captured once refreshes the cached
-    MXFP8 weight when the flag is 0 and keeps it when it is 1 (TE PR #3264,
-    review: skipped cached updates during CUDA-graph replay)."""
-    x1 = syn.normal_bf16(384, 1024, seed=41)
-    x2 = syn.normal_bf16(384, 1024, seed=42)
+    weight -- MXFP8 rowwise, MXFP8 columnwise, 128x128 blockwise and packed
+    MXFP4 -- when the flag is 0 and keeps every byte when it is 1 (TE PR
+    #3264, review: skipped cached updates during CUDA-graph replay)."""
+    R, K = 384, 1024
+    x1 = syn.normal_bf16(R, K, seed=41)
+    x2 = syn.normal_bf16(R, K, seed=42)
     x = dev_bf16(x1)
     skip = torch.zeros(1, dtype=torch.int32, device="cuda")
-    d = torch.empty((384, 1024), dtype=torch.uint8, device="cuda")
-    s = torch.empty(mx.scale_bytes(384, 1024, "swizzled"), dtype=torch.uint8, device="cuda")
-    bd = torch.empty((384, 1024), dtype=torch.uint8, device="cuda")
-    bs = torch.empty(mx.tile_scale_count(384, 1024), dtype=torch.float32, device="cuda")
+    d = torch.empty((R, K), dtype=torch.uint8, device="cuda")
+    s = torch.empty(mx.scale_bytes(R, K, "swizzled"), dtype=torch.uint8, device="cuda")
+    cd = torch.empty((R, K), dtype=torch.uint8, device="cuda")
+    cs = torch.empty(mx.scale_bytes(K, R, "swizzled"), dtype=torch.uint8, device="cuda")
+    bd = torch.empty((R, K), dtype=torch.uint8, device="cuda")
+    bs = torch.empty(mx.tile_scale_count(R, K), dtype=torch.float32, device="cuda")
+    pk = torch.empty((R, K // 2), dtype=torch.uint8, device="cuda")
+    ps = torch.empty(mx.scale_bytes(R, K, "swizzled"), dtype=torch.uint8, device="cuda")
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
-        calls = [mx.plan_mxfp8_row_direct(x, "swizzled", d, s, skip=skip), mx.plan_fp8_block128_direct(x, bd, bs, skip=skip)]
+        calls = [mx.plan_mxfp8_row_direct(x, "swizzled", d, s, skip=skip),
+                 mx.plan_mxfp8_col_direct(x, "swizzled", cd, cs, skip=skip),
+                 mx.plan_fp8_block128_direct(x, bd, bs, skip=skip),
+                 mx.plan_mxfp4_pack(x, "swizzled", pk, ps, skip=skip)]
         for c in calls:
             c()
         side.synchronize()
@@ -681,27 +720,30 @@ def test_skip_flag_in_a_captured_graph(mx):
             for c in calls:
                 c()
     torch.cuda.current_stream().wait_stream(side)
+    outs = (d, s, cd, cs, bd, bs, pk, ps)
 
     def want(xn):
         rd, rs = oracle.mxfp8_row_direct(xn, oracle.SWIZZLED)
+        rcd, rcs = oracle.mxfp8_col_direct(xn, oracle.SWIZZLED)
         bdd, bss = oracle.fp8_block128_direct(xn)
-        return rd, rs, bdd, bss.view(np.uint32).reshape(-1)
+        rpk, rps = oracle.mxfp4_pack(xn, oracle.SWIZZLED)
+        return rd, rs, rcd, rcs, bdd, bss.view(np.uint32).reshape(-1), rpk, rps
 
     g.replay()
     torch.cuda.synchronize()
     w1 = want(x1)
-    for got, ref in zip((d, s, bd, bs), w1):
+    for got, ref in zip(outs, w1):
         np.testing.assert_array_equal(host_bits(got), ref)
     x.copy_(dev_bf16(x2))
     skip.fill_(1)
     g.replay()
     torch.cuda.synchronize()
-    for got, ref in zip((d, s, bd, bs), w1):  # kept
+    for got, ref in zip(outs, w1):  # kept
         np.testing.assert_array_equal(host_bits(got), ref)
     skip.zero_()
     g.replay()
     torch.cuda.synchronize()
-    for got, ref in zip((d, s, bd, bs), want(x2)):  # refreshed
+    for got, ref in zip(outs, want(x2)):  # refreshed
         np.testing.assert_array_equal(host_bits(got), ref)
 
 
@@ -795,3 +837,34 @@ def test_fast_math_build_gives_identical_bytes(mx):
             K = x.shape[-1]
             assert torch.equal(lib_a.dequantize(pa, scales=qa, layout="swizzled", mxfp4_K=K).view(torch.int16),
                                lib_b.dequantize(pb, scales=qb, layout="swizzled", mxfp4_K=K).view(torch.int16))
+
+
+def test_binding_rejects_short_buffers(mx):
+    """The binding refuses, before any launch, scale buffers shorter than
+    their layout, a tile-scale tensor of the wrong dtype or count, and a
+    grouped export spread over tensors it cannot address (the C ABI sees
+    only pointers, so these would be reads past a buffer's end)."""
+    rows, K = 200, 7184
+    x = dev_bf16(syn.normal_bf16(rows, K, seed=90))
+    d, s = mx.mxfp8_row_direct(x, "swizzled")
+    compact = s.reshape(-1)[: rows * 225].clone()
+    with pytest.raises(ValueError):
+        mx.dequantize(d, scales=compact, layout="swizzled")
+    with pytest.raises(ValueError):
+        mx.export_mxfp8(d, compact, shape=(rows, K), layout="swizzled")
+    with pytest.raises(ValueError):
+        mx.export_mxfp8_grouped([{"data": d, "scales": compact, "shape": (rows, K), "layout": "swizzled"}])
+    cd, cs = mx.mxfp8_col_direct(x, "swizzled")
+    with pytest.raises(ValueError):  # columnwise scales are sized for the transposed matrix
+        mx.dequantize(cd, scales=cs.reshape(-1)[: mx.scale_bytes(K, rows, "compact") - 1].clone(), layout="compact",
+                      columnwise=True)
+    bd, bs = mx.fp8_block128_direct(x)
+    with pytest.raises(ValueError):
+        mx.dequantize(bd, tile_scale_inv=bs.half())
+    with pytest.raises(ValueError):
+        mx.dequantize(bd, tile_scale_inv=bs.reshape(-1)[:-1].clone())
+    # the valid calls still run and agree
+    a = mx.dequantize(d, scales=s, layout="swizzled")
+    b = mx.dequantize(d, scales=mx.mxfp8_row_direct(x, "compact")[1], layout="compact")
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
