@@ -466,11 +466,13 @@ class Library:
         call()
         return comp
 
-    def export_mxfp8_grouped(self, storages, scale_out: Optional[torch.Tensor] = None):
+    def plan_export_mxfp8_grouped(self, storages, scale_out: Optional[torch.Tensor] = None):
         """Export many MXFP8 storages at once.  ``storages`` is a list of
         dicts with keys data, scales, shape, layout (default compact) and fp8
         (default e4m3).  The copies share ``scale_out`` (allocated when None)
-        and run in one launch per 128 storages.  Returns MXFP8Components."""
+        and run in one launch per 128 storages.  Returns (Call, list of
+        MXFP8Components); the components' scales are valid once the Call has
+        run."""
         n = len(storages)
         st = (_Storage * max(n, 1))()
         sizes, keep = [], []
@@ -508,12 +510,6 @@ class Library:
         if scale_out is None and need:
             scale_out = torch.empty(need, dtype=torch.uint8, device=dev)
         comps = (_Components * max(n, 1))()
-        if n:
-            with torch.cuda.device(dev):
-                self._check(self.L.mxq_export_mxfp8_grouped(
-                    st, n, ctypes.c_void_p(scale_out.data_ptr()) if scale_out is not None else None,
-                    scale_out.numel() if scale_out is not None else 0, comps, _stream(keep[0][1])),
-                    "mxq_export_mxfp8_grouped")
         out, off = [], 0
         for g, (shape, rows, nb, view) in enumerate(sizes):
             data, scales = keep[g]
@@ -524,13 +520,27 @@ class Library:
             else:
                 sc = scale_out[off: off + rows * nb].view(shape[:-1] + (nb,))
                 off += rows * nb
-            out.append(MXFP8Components(values, sc, bool(comps[g].is_view)))
+            out.append(MXFP8Components(values, sc, view))
+        if not n:
+            return Call(self, None, (), "mxq_export_mxfp8_grouped", (), None), out
+        args = (st, n, ctypes.c_void_p(scale_out.data_ptr()) if scale_out is not None else None,
+                scale_out.numel() if scale_out is not None else 0, comps, _stream(keep[0][1]))
+        return Call(self, self.L.mxq_export_mxfp8_grouped, args, "mxq_export_mxfp8_grouped",
+                    (keep, scale_out, st, comps), dev), out
+
+    def export_mxfp8_grouped(self, storages, scale_out: Optional[torch.Tensor] = None):
+        """Eager form of plan_export_mxfp8_grouped: runs the copies and
+        returns the list of MXFP8Components."""
+        call, out = self.plan_export_mxfp8_grouped(storages, scale_out)
+        call()
         return out
 
-    def quantize_export_mxfp8(self, x: torch.Tensor, data: Optional[torch.Tensor] = None,
-                              scales: Optional[torch.Tensor] = None) -> MXFP8Components:
-        """Quantize x (bf16/fp32) to MXFP8 rowwise (direct lift) and return the
-        exported values and compact scales in one call."""
+    def plan_quantize_export_mxfp8(self, x: torch.Tensor, data: Optional[torch.Tensor] = None,
+                                   scales: Optional[torch.Tensor] = None):
+        """Quantize x (bf16/fp32) to MXFP8 rowwise (direct lift) and export it
+        in one call.  Returns (Call, MXFP8Components): the values and compact
+        scales are views of ``data`` and ``scales``, valid once the Call has
+        run."""
         _need_cuda(x, data, scales)
         dt = _dt_code(x)
         rows, K, ldx = _rows_view(x)
@@ -539,16 +549,23 @@ class Library:
             data = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
         if scales is None:
             scales = torch.empty(tuple(x.shape[:-1]) + (nb,), dtype=torch.uint8, device=x.device)
-        if not data.is_contiguous() or data.numel() != rows * K or not scales.is_contiguous() or scales.numel() < rows * nb:
-            raise ValueError("data must be rows*K contiguous bytes and scales rows*ceil(K/32)")
+        if not data.is_contiguous() or data.numel() != rows * K or data.dtype != torch.uint8:
+            raise ValueError("data must be a contiguous uint8 tensor of rows*K bytes")
+        _check_bytes(scales, rows * nb, "scales", "rows*ceil(K/32)")
         comp = _Components()
-        with torch.cuda.device(x.device):
-            self._check(self.L.mxq_quantize_export_mxfp8(ctypes.c_void_p(x.data_ptr()), dt, rows, K, ldx,
-                                                         ctypes.c_void_p(data.data_ptr()),
-                                                         ctypes.c_void_p(scales.data_ptr()), ctypes.byref(comp),
-                                                         _stream(x)), "mxq_quantize_export_mxfp8")
-        return MXFP8Components(data.view(torch.float8_e4m3fn).view(x.shape),
-                               scales.reshape(-1)[: rows * nb].view(tuple(x.shape[:-1]) + (nb,)), True)
+        args = (ctypes.c_void_p(x.data_ptr()), dt, rows, K, ldx, ctypes.c_void_p(data.data_ptr()),
+                ctypes.c_void_p(scales.data_ptr()), ctypes.byref(comp), _stream(x))
+        call = Call(self, self.L.mxq_quantize_export_mxfp8, args, "mxq_quantize_export_mxfp8",
+                    (x, data, scales, comp), x.device)
+        return call, MXFP8Components(data.view(torch.float8_e4m3fn).view(x.shape),
+                                     scales.reshape(-1)[: rows * nb].view(tuple(x.shape[:-1]) + (nb,)), True)
+
+    def quantize_export_mxfp8(self, x: torch.Tensor, data: Optional[torch.Tensor] = None,
+                              scales: Optional[torch.Tensor] = None) -> MXFP8Components:
+        """Eager form of plan_quantize_export_mxfp8."""
+        call, comp = self.plan_quantize_export_mxfp8(x, data, scales)
+        call()
+        return comp
 
 
 class Call:
@@ -560,6 +577,8 @@ class Call:
         self.lib, self.fn, self.args, self.name, self.keep, self.device = lib, fn, args, name, keep, device
 
     def __call__(self) -> None:
+        if self.fn is None:  # nothing to launch (an empty grouped export)
+            return
         if torch.cuda.current_device() != self.device.index:
             with torch.cuda.device(self.device):
                 status = self.fn(*self.args)

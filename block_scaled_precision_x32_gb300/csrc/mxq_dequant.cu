@@ -18,8 +18,10 @@
 // is exact whenever the product stays normal (code >= 10 for E4M3, >= 17 for
 // E5M2).  Blocks with a NaN or Inf payload, scale code 255, or a smaller
 // code for fp32 output take the element-wise fp32 path, which also makes
-// NaN canonical.  The 128x128 form multiplies by an arbitrary fp32
-// scale_inv and always takes the fp32 path.  Packed MXFP4 (16 bytes of
+// NaN canonical.  The 128x128 form takes the same fast path when its tile
+// scale_inv is a power of two 2^T (what the converter writes: its exponent
+// field is the code T + 127) and the element-wise fp32 path for any other
+// fp32 scale_inv.  Packed MXFP4 (16 bytes of
 // nibbles per block) maps each E2M1 code to its bf16 pattern and scales it
 // by 2^(code-127) with one exact bf16 multiply (Inf past the range; the
 // value is exact in bf16 otherwise, 2^-128 included, so fp32 output is the
@@ -192,9 +194,22 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a, int64_
             scale16 = bf16_scale_pair(c);
         } else {
             scale32 = reinterpret_cast<const uint32_t*>(a.tile_scale_inv)[(r >> 7) * tc + (col0 >> 7)];
+            // The converter writes tile_scale_inv = 2^T, T in [-127, 127]: the
+            // exponent field of a normal 2^T is the UE8M0 code T + 127 (2^-127 is
+            // the subnormal 0x00400000, code 0), and the placement decode of the
+            // MXFP8 form applies unchanged.  Any other scale_inv takes the
+            // element-wise fp32 path.
+            const uint32_t ex = scale32 >> 23;  // sign and exponent field
+            const bool pow2 = scale32 == 0x00400000u || ((scale32 & 0x007FFFFFu) == 0u && ex >= 1u && ex <= 254u);
+            const uint32_t c = scale32 == 0x00400000u ? 0u : ex;
+            uint32_t sp = 0u;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sp |= special_bytes<false>(w[k]);
+            fast = pow2 && sp == 0u && (BF16OUT || c >= 10u);
+            scale16 = bf16_scale_pair(c);
         }
         uint32_t o[WORDS];
-        if (KIND == 0 && fast) {
+        if (fast) {
             const uint32_t fix = E5M2 ? 0x77807780u : 0x7B807B80u;  // 2^112 / 2^120, both halves
 #pragma unroll
             for (int k = 0; k < 8; ++k) {

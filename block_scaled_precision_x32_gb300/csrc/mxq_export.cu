@@ -5,22 +5,29 @@
 // scales are copied only when padded in the last dimension or swizzled for
 // GEMM, padding dropped and the swizzle undone.
 //
-// Swizzled input: one CTA per (128-row tile, group of 16 column tiles).
-// The group's bytes are contiguous in the swizzled buffer (16 x 512), so
-// they are staged in shared memory with 16-byte loads -- each 512-byte tile
+// Swizzled input, nb >= 16, scales and output 16-byte aligned (the usual
+// case: every GEMM-swizzled weight with K >= 512): the chunk kernel below,
+// which needs no shared memory -- each lane turns 16-byte loads of four rows'
+// scales into aligned 16-byte chunks of those rows' compact output.
+// Other swizzled input: one CTA per (128-row tile, group of 16 column
+// tiles).  The group's bytes are contiguous in the swizzled buffer (16 x 512),
+// so they are staged in shared memory with 16-byte loads -- each 512-byte tile
 // padded by one word so that lanes reading the same word of consecutive
 // tiles hit distinct banks -- and written out row by row, consecutive lanes
-// on consecutive output words (4 scales) or bytes.
-// Swizzled input with nb % 4 != 0 (compact rows are not whole words): one CTA
-// per 128-row tile stages all of the tile's column tiles, and writes the
-// tile's compact output -- one contiguous range -- as aligned words.
+// on consecutive output words (4 scales) or bytes.  With nb % 4 != 0 and an
+// output that is not 16-byte aligned: one CTA per 128-row tile stages all of
+// the tile's column tiles and writes its compact output -- one contiguous
+// range -- as aligned words.
 // Padded input: one warp per row, lanes on consecutive bytes.
 // Grouped export: up to kGroupedMax storages per launch, their descriptors
-// passed by value in the kernel parameters.
+// passed by value in the kernel parameters; chunk-path storages run the chunk
+// kernel's code, the others a byte copy; every storage's row tiles are walked
+// with a grid stride.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 
+#include "mxq_device.cuh"
 #include "mxq_internal.h"
 
 namespace mxq {
@@ -199,6 +206,117 @@ __global__ void __launch_bounds__(kFlatThreads) unswizzle_flat_kernel(ExportArgs
     }
 }
 
+// Swizzled input and compact output both 16-byte aligned, nb >= 16 (any
+// nb % 4): no shared memory.  In the swizzled layout the 16 bytes at
+// (column tile jt, q) -- offset 512 jt + 16 q of a row tile -- are the
+// scales of rows q, q + 32, q + 64, q + 96 at columns 4 jt .. 4 jt + 3, one
+// word per row; lane q of a warp owns those four rows, so every 16-byte load
+// feeds four rows.  Compact row r starts at byte r nb and the four rows of a
+// lane start at the same offset mod 16 (32 nb is a multiple of 16), so with
+// b = (-q nb) mod 16 chunk i of each row -- row bytes [b + 16 i, b + 16 i + 16)
+// -- is one aligned 16-byte store: the words of column tiles
+// 4 i + b / 4 .. 4 i + b / 4 + 4, funnel-shifted by b % 4 bytes.  A row's first
+// b bytes close the previous row's last chunk, which takes them from the
+// first 16 bytes of its next row (column tiles 0..3 of lane q + 1; a lane
+// q = 31 row ends on a 16-byte boundary, as does every row tile).  Since
+// nb >= 16 a chunk spans at most two rows.  A warp takes CPW consecutive
+// chunks of every row of its lane (chunk group cg); the next chunk's four
+// loads are issued before the current chunk is stored.  Only the last row of
+// a tensor whose compact end is not 16-byte aligned stores bytes.
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int s) {
+    return s == 0 ? v.x : s == 1 ? v.y : s == 2 ? v.z : v.w;
+}
+
+// Bytes [0, e) of o followed by bytes [0, 16 - e) of h, e in 1..15.
+__device__ __forceinline__ void merge_next_row(uint32_t (&o)[4], const uint32_t (&h)[4], int e) {
+    const int ea = e >> 2, ec = 8 * (e & 3);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int k = t - ea;  // h word holding byte 4 t - e + 3
+        const uint32_t hi = k == 0 ? h[0] : k == 1 ? h[1] : k == 2 ? h[2] : k == 3 ? h[3] : 0u;
+        const uint32_t lo = k == 1 ? h[0] : k == 2 ? h[1] : k == 3 ? h[2] : 0u;
+        const uint32_t hs = __funnelshift_l(lo, hi, ec);  // bytes 4 t - e .. 4 t - e + 3 of h
+        const int keep = min(max(e - 4 * t, 0), 4);       // bytes of this word still from o
+        const uint32_t m = keep == 4 ? 0xFFFFFFFFu : (1u << (8 * keep)) - 1u;
+        o[t] = (o[t] & m) | (hs & ~m);
+    }
+}
+
+constexpr int kChunkThreads = 128;
+
+// Chunk group cg (chunks CPW cg .. CPW cg + CPW - 1) of row tile rt, whose
+// ct * 512 swizzled bytes start at `tile`.
+template <int CPW>
+__device__ __forceinline__ void unswizzle_chunks(const ExportArgs& a, int64_t rt, int cg, const uint8_t* tile) {
+    const int64_t nb = (a.K + 31) >> 5, ct = (nb + 3) >> 2;
+    const int q = threadIdx.x & 31;
+    const int n16 = (int)(nb & 15);
+    const int b = (16 - ((q * n16) & 15)) & 15;
+    const int ab = b >> 2, sh = 8 * (b & 3);
+    const int e = 16 - ((16 - (((q + 1) * n16) & 15)) & 15);  // bytes of the last chunk inside the row
+    const int64_t ilast = (nb - 1 - b) >> 4;                     // last chunk of each of the lane's rows
+    const int64_t i0 = (int64_t)cg * CPW;
+    const uint8_t* src = tile + 16 * q;
+    const int64_t r0 = rt * 128;
+    const int nrows = (int)min((int64_t)128, a.rows - r0);
+    auto tile_at = [&](int64_t jt) -> uint4 {
+        return jt < ct ? *reinterpret_cast<const uint4*>(src + jt * 512) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    uint4 w[5];
+#pragma unroll
+    for (int t = 0; t < 5; ++t) w[t] = tile_at(4 * i0 + ab + t);
+#pragma unroll
+    for (int c = 0; c < CPW; ++c) {
+        const int64_t i = i0 + c;
+        if (i > ilast) break;
+        uint4 nw[4];
+        if (c + 1 < CPW) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) nw[t] = tile_at(4 * (i + 1) + ab + 1 + t);
+        }
+        const bool cross = i == ilast && e < 16;
+        uint4 h[4];
+        if (cross) {  // the next rows' first 16 bytes: column tiles 0..3 of lane q + 1 (q < 31 here)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) h[t] = *reinterpret_cast<const uint4*>(src + t * 512 + 16);
+        }
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const int rr = q + 32 * s;
+            if (rr >= nrows) break;
+            uint32_t o[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) o[t] = __funnelshift_r(word_of(w[t], s), word_of(w[t + 1], s), sh);
+            uint8_t* dst = a.out + (r0 + rr) * nb + b + 16 * i;
+            if (cross) {
+                const uint32_t hw[4] = {word_of(h[0], s), word_of(h[1], s), word_of(h[2], s), word_of(h[3], s)};
+                merge_next_row(o, hw, e);
+                if (rr + 1 >= nrows) {  // the tensor's last row: its chunk stops at the end of the output
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        if (k < e) dst[k] = (uint8_t)(o[k >> 2] >> (8 * (k & 3)));
+                    continue;
+                }
+            }
+            st16(dst, o[0], o[1], o[2], o[3]);
+        }
+        if (c + 1 < CPW) {
+            w[0] = w[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) w[t + 1] = nw[t];
+        }
+    }
+}
+
+template <int CPW>
+__global__ void __launch_bounds__(kChunkThreads) unswizzle_chunk_kernel(ExportArgs a, int64_t tiles_r, int ngroups) {
+    const int cg = (int)blockIdx.y * (kChunkThreads / 32) + (int)(threadIdx.x >> 5);
+    if (cg >= ngroups) return;
+    const int64_t ct = (((a.K + 31) >> 5) + 3) >> 2;
+    for (int64_t rt = blockIdx.x; rt < tiles_r; rt += gridDim.x)
+        unswizzle_chunks<CPW>(a, rt, cg, a.scales + rt * ct * 512);
+}
+
 // Largest staging area of the flat kernel (bytes of dynamic shared memory).
 constexpr int kFlatSmemMax = 160 * 1024;
 
@@ -217,20 +335,36 @@ __global__ void __launch_bounds__(kThreads) unpad_kernel(ExportArgs a) {
     unpad_rows(a, 0, a.rows, warp, nwarps);
 }
 
-// Many storages in one launch: blockIdx.z picks the storage, (x, y) its
-// column group and 128-row tile; CTAs outside a storage's extent return.
-__global__ void __launch_bounds__(kThreads) grouped_export_kernel(GroupedExport b) {
-    __shared__ uint32_t tile[kGroup * kTileWords];
+// Many storages in one launch: blockIdx.z picks the storage, blockIdx.x
+// walks its 128-row tiles (grid stride, so any number of them), blockIdx.y
+// its chunk groups.  A storage the chunk path takes (the host sets path 1:
+// swizzled, nb >= 16, 16-byte aligned scales and output) runs it as the
+// single export does; any other swizzled or padded storage is copied byte by
+// byte by the blockIdx.y == 0 CTAs.
+template <int CPW>
+__global__ void __launch_bounds__(kChunkThreads) grouped_export_kernel(GroupedExport b) {
     const ExportArgs& a = b.item[blockIdx.z];
-    const int64_t nb = (a.K + 31) >> 5;
-    const int64_t rt = blockIdx.y, tr = (a.rows + 127) >> 7;
-    if (rt >= tr) return;
-    if (a.lay == 2) {
-        const int64_t ct = ((nb + 3) >> 2), jt0 = (int64_t)blockIdx.x * kGroup;
-        if (jt0 >= ct) return;
-        unswizzle_group<false, false>(a, rt, jt0, tile);
-    } else if (blockIdx.x == 0) {
-        unpad_rows(a, rt * 128, min(a.rows, rt * 128 + 128), threadIdx.x >> 5, kThreads / 32);
+    const int64_t nb = (a.K + 31) >> 5, Cp = (nb + 3) & ~int64_t(3);
+    const int64_t tr = (a.rows + 127) >> 7;
+    if (a.path == 1) {
+        const int64_t ngroups = ((nb + 15) / 16 + CPW - 1) / CPW;
+        const int64_t cg = (int64_t)blockIdx.y * (kChunkThreads / 32) + (threadIdx.x >> 5);
+        if (cg >= ngroups) return;
+        const int64_t ct = Cp >> 2;
+        for (int64_t rt = blockIdx.x; rt < tr; rt += gridDim.x)
+            unswizzle_chunks<CPW>(a, rt, (int)cg, a.scales + rt * ct * 512);
+        return;
+    }
+    if (blockIdx.y != 0) return;
+    for (int64_t rt = blockIdx.x; rt < tr; rt += gridDim.x) {
+        const int64_t r0 = rt * 128, n = min((int64_t)128, a.rows - r0) * nb;
+        for (int64_t f = threadIdx.x; f < n; f += kChunkThreads) {
+            const int64_t r = r0 + f / nb, j = f % nb;
+            const int64_t off = a.lay == 2 ? ((r >> 7) * (Cp >> 2) + (j >> 2)) * 512 + (r & 31) * 16 +
+                                                 ((r >> 5) & 3) * 4 + (j & 3)
+                                           : r * Cp + j;
+            a.out[r * nb + j] = a.scales[off];
+        }
     }
 }
 
@@ -253,12 +387,51 @@ cudaError_t launch_flat(const ExportArgs& a, int64_t tr, int64_t grid, int64_t s
 }
 }  // namespace
 
+// The chunk path of a swizzled export: nb >= 16 and 16-byte aligned
+// scales and output.  Chunks per warp (CPW), measured on GB300: 2 for small
+// exports (up to 8 such warps per SM; 8192 x 8192: 2.3 us against 2.6 us at
+// 1), else 1 (the 32 x 4096 x 7184 MoE stack: 13.6 us against 14.4 us at 2
+// and 14.2 us at 4 or 8).  Also measured and dropped: 32-byte chunks (whole
+// sector stores; 150+ registers, 20.9 us against 16.9 us for that build's
+// 16-byte chunks), row tiles staged through a ring of shared-memory stages by
+// cp.async (barrier-bound, 24 us) and persistent warps with the next unit's
+// loads in flight (13.44 us, no gain).
+struct ChunkPlan {
+    bool ok;
+    int cpw;
+    int64_t nc;  // 16-byte chunks per compact row, at most
+};
+
+static ChunkPlan chunk_plan(const ExportArgs& a) {
+    ChunkPlan p{false, 1, 0};
+    const int64_t nb = ceil_div(a.K, 32);
+    if (a.lay != 2 || nb < 16 || (reinterpret_cast<uintptr_t>(a.scales) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(a.out) & 15) != 0)
+        return p;
+    p.nc = ceil_div(nb, 16);
+    if (ceil_div(p.nc, kChunkThreads / 32) > 65535) return p;  // grid y holds the chunk groups
+    p.ok = true;
+    p.cpw = ceil_div(a.rows, 128) * p.nc <= (int64_t)sm_count() * 8 ? 2 : 1;
+    return p;
+}
+
+template <int CPW>
+static cudaError_t launch_chunks(const ExportArgs& a, int64_t tr, int64_t nc, cudaStream_t s) {
+    const int64_t ngroups = ceil_div(nc, CPW);
+    const int64_t gy = ceil_div(ngroups, kChunkThreads / 32);
+    const int64_t gx = tr < 65535 ? tr : 65535;
+    unswizzle_chunk_kernel<CPW><<<dim3((unsigned)gx, (unsigned)gy), kChunkThreads, 0, s>>>(a, tr, (int)ngroups);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_export(const ExportArgs& a, cudaStream_t s) {
     const int64_t nb = ceil_div(a.K, 32);
     if (a.lay == 2) {
         const int64_t ct = ceil_div(nb, 4);
         const int64_t tr = ceil_div(a.rows, 128);
         const bool vin = (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0;
+        const ChunkPlan p = chunk_plan(a);
+        if (p.ok) return p.cpw == 1 ? launch_chunks<1>(a, tr, p.nc, s) : launch_chunks<2>(a, tr, p.nc, s);
         const int64_t smem = (ct + 1) * kTileWords * 4 + ((nb + 3) & ~int64_t(3)) * 4;
         // nb > 4: a word of compact output then meets at most one row boundary
         if (nb % 4 != 0 && nb > 4 && vin && smem <= kFlatSmemMax) {
@@ -289,16 +462,32 @@ cudaError_t launch_export(const ExportArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_export_grouped(const GroupedExport& b, cudaStream_t s) {
-    if (b.count <= 0) return cudaSuccess;
-    int64_t gx = 1, gy = 1;
+// The grouped kernel runs one CPW for all of its chunk-path storages.
+cudaError_t launch_export_grouped(const GroupedExport& b0, cudaStream_t s) {
+    if (b0.count <= 0) return cudaSuccess;
+    GroupedExport b = b0;
+    int64_t gx = 1, gy = 1, warps1 = 0;
     for (int i = 0; i < b.count; ++i) {
-        const int64_t nb = ceil_div(b.item[i].K, 32);
-        gx = std::max(gx, ceil_div(ceil_div(nb, 4), kGroup));
-        gy = std::max(gy, ceil_div(b.item[i].rows, 128));
+        ExportArgs& a = b.item[i];
+        const ChunkPlan p = chunk_plan(a);
+        a.path = p.ok ? 1 : 0;
+        gx = std::max(gx, ceil_div(a.rows, 128));
+        if (p.ok) warps1 += ceil_div(a.rows, 128) * p.nc;
     }
-    if (gy > 65535) return cudaErrorInvalidValue;
-    grouped_export_kernel<<<dim3((unsigned)gx, (unsigned)gy, (unsigned)b.count), kThreads, 0, s>>>(b);
+    const int cpw = warps1 <= (int64_t)sm_count() * 8 ? 2 : 1;
+    for (int i = 0; i < b.count; ++i) {
+        const ExportArgs& a = b.item[i];
+        if (a.path == 1) gy = std::max(gy, ceil_div(ceil_div(ceil_div(ceil_div(a.K, 32), 16), cpw), kChunkThreads / 32));
+    }
+    // every storage's tiles are walked with a grid stride: a cap on gx only
+    // bounds the launch, not the sizes it can copy
+    const int64_t cap = (int64_t)sm_count() * 64;
+    if (gx > cap) gx = cap;
+    const dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)b.count);
+    if (cpw == 1)
+        grouped_export_kernel<1><<<grid, kChunkThreads, 0, s>>>(b);
+    else
+        grouped_export_kernel<2><<<grid, kChunkThreads, 0, s>>>(b);
     return cudaGetLastError();
 }
 

@@ -53,6 +53,7 @@ struct DequantArgs {
 struct ExportArgs {
     const uint8_t* scales;
     int lay;
+    int path;  // grouped export only: 1 = the chunk kernel's path (set by the launcher)
     int64_t rows, K;
     uint8_t* out;  // compact [rows, nb]
 };

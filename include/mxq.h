@@ -273,11 +273,14 @@ MXQ_API mxq_status mxq_export_mxfp8(const mxq_mxfp8_storage* st, uint8_t* scale_
  * per-expert export of a GroupedTensor as not covered there) in as few
  * launches as possible: every storage is exported as by mxq_export_mxfp8;
  * the ones that need a copy get consecutive regions of scale_out, in order,
- * and all copies run in one kernel launch per 128 storages.
+ * and all copies run in one kernel launch per 128 storages.  Storages of
+ * any size are accepted (each one's 128-row tiles are walked in a loop).
  *   st[count], out[count]: storages and their components.
  *   scale_out: device buffer for the copied scales, scale_out_bytes long.
- * Errors: as mxq_export_mxfp8 for any storage (checked before anything is
- * launched); BUFFER_TOO_SMALL if the copies do not fit. */
+ * Errors: as mxq_export_mxfp8 for any storage, and BUFFER_TOO_SMALL if the
+ * copies do not fit -- both checked before anything is launched; MXQ_ERR_CUDA
+ * if a launch fails, in which case the launches of earlier groups of 128
+ * storages may already be enqueued. */
 MXQ_API mxq_status mxq_export_mxfp8_grouped(const mxq_mxfp8_storage* st, int64_t count, uint8_t* scale_out,
                                             size_t scale_out_bytes, mxq_mxfp8_components* out, cudaStream_t stream);
 

@@ -350,6 +350,33 @@ def test_dequant_block128_arbitrary_scales(mx):
         np.testing.assert_array_equal(host_bits(got), oracle_bits(oracle.dequant_block128(data, sinv, ocode)))
 
 
+@pytest.mark.parametrize("K", [256, 272])
+def test_dequant_block128_power_of_two_scales(mx, K):
+    """Blockwise dequantize of every payload byte with tile scales 2^T over
+    the whole range the converter writes -- 2^-127 (the fp32 subnormal), the
+    fp32-output boundary 2^-118 / 2^-117, 2^-1, 2^0, 2^7, 2^127 -- and with
+    scales just off a power of two, -2^T, +-Inf and NaN beside them (the
+    element-wise path).  K = 256 takes the vector path, K = 272 the ragged
+    one; rows of a 128-row tile mix NaN payloads (0x7F, 0xFF) with others."""
+    scales_t = [-127, -118, -117, -1, 0, 7, 127]
+    odd = [np.float32(1.5), np.float32(-1.0), np.float32(np.inf), np.float32(-np.inf), np.float32(np.nan),
+           np.float32(np.ldexp(1.0, -120) * 1.25)]
+    sinv_list = [np.float32(np.ldexp(1.0, t)) for t in scales_t] + odd
+    rows = 128 * len(sinv_list)
+    tc = (K + 127) // 128
+    data = np.tile(np.arange(256, dtype=np.uint8), rows * K // 256 + 1)[: rows * K].reshape(rows, K)
+    data = np.ascontiguousarray(np.roll(data, 5, axis=1))
+    sinv = np.empty((len(sinv_list), tc), dtype=np.float32)
+    for i, v in enumerate(sinv_list):
+        sinv[i, :] = v
+    d = torch.from_numpy(data).cuda()
+    s = torch.from_numpy(sinv).cuda()
+    for odt, ocode in ((torch.float32, oracle.FP32), (torch.bfloat16, oracle.BF16)):
+        got = mx.dequantize(d, tile_scale_inv=s, out_dtype=odt)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host_bits(got), oracle_bits(oracle.dequant_block128(data, sinv, ocode)))
+
+
 # ------------------------------------------- full-size workloads, sampled
 
 def _sample_rows(rows, n, seed):
@@ -585,6 +612,89 @@ def test_export_wide_rows(mx, K):
     np.testing.assert_array_equal(host_bits(off.scale_inv).reshape(rows, nb), want)
     r = host_bits(raw)
     assert r[0] == 0xA5 and (r[1 + rows * nb:] == 0xA5).all()
+
+
+def _random_swizzled(rows, K, seed):
+    """A swizzled scale buffer of random bytes, padding included (an export
+    must never read the padding into its output)."""
+    n = oracle.scale_bytes(rows, K, oracle.SWIZZLED)
+    return np.random.default_rng(seed).integers(0, 256, size=n, dtype=np.uint8)
+
+
+@pytest.mark.parametrize("rows", [1, 31, 127, 128, 129, 300])
+def test_export_chunk_path_every_scale_count(mx, rows):
+    """Swizzled -> compact export over scale counts 16..70, 100, 225, 256,
+    1023 (every nb % 16, nb % 4 and row offset mod 16), ragged last row
+    tiles, random bytes in the padding: equal to the oracle's export.  Also
+    into outputs 1, 4 and 8 bytes off a 16-byte boundary (the word and byte
+    kernels)."""
+    for nb in list(range(16, 71)) + [100, 225, 256, 1023]:
+        K = 32 * nb - (7 if nb % 3 == 0 else 0)
+        sw = _random_swizzled(rows, K, seed=rows * 10000 + nb)
+        want = oracle.export_scales(sw, oracle.SWIZZLED, rows, K)
+        d = torch.from_numpy(sw).cuda()
+        comp = mx.export_mxfp8(torch.empty((rows, K), dtype=torch.uint8, device="cuda"), d, shape=(rows, K),
+                               layout="swizzled")
+        outs = [comp.scale_inv]
+        if nb in (16, 17, 225):
+            for off in (1, 4, 8):
+                raw = torch.full((rows * nb + 32,), 0xA5, dtype=torch.uint8, device="cuda")
+                c = mx.export_mxfp8(torch.empty((rows, K), dtype=torch.uint8, device="cuda"), d, shape=(rows, K),
+                                    layout="swizzled", scale_out=raw[off:off + rows * nb])
+                outs.append(c.scale_inv)
+                torch.cuda.synchronize()
+                r = host_bits(raw)
+                assert (r[:off] == 0xA5).all() and (r[off + rows * nb:] == 0xA5).all()
+        torch.cuda.synchronize()
+        for o in outs:
+            np.testing.assert_array_equal(host_bits(o).reshape(rows, nb), want, err_msg=f"rows {rows} nb {nb}")
+
+
+@pytest.mark.parametrize("nb", [16, 17, 63, 225, 256, 300, 600, 1023])
+def test_export_staged_pipeline(mx, nb):
+    """Exports of more than two row tiles per SM take the persistent kernel
+    that stages row tiles in shared memory (7, 4 or 2 stages by tile size;
+    nb = 1023 no longer fits and takes the chunk kernel): random swizzled
+    bytes, a ragged last row tile, equal to the oracle's export."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = (2 * sms + 1) * 128 + 77
+    K = 32 * nb - 5
+    sw = _random_swizzled(rows, K, seed=nb)
+    d = torch.from_numpy(sw).cuda()
+    comp = mx.export_mxfp8(torch.empty((rows, K), dtype=torch.uint8, device="cuda"), d, shape=(rows, K),
+                           layout="swizzled")
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host_bits(comp.scale_inv).reshape(rows, nb),
+                                  oracle.export_scales(sw, oracle.SWIZZLED, rows, K))
+
+
+def test_export_chunk_path_past_65535_row_tiles(mx):
+    """8,388,736 rows x 16 scale columns (65,537 row tiles of random
+    swizzled bytes, 134 MB): the chunk kernel's grid walks the row tiles,
+    as does the grouped kernel with the same storage beside two small ones;
+    sampled tiles against the oracle, grouped against single over all."""
+    rows, K = 65537 * 128, 512
+    nb = 16
+    sw = _random_swizzled(rows, K, seed=65537)
+    d = torch.from_numpy(sw).cuda()
+    payload = torch.empty((rows, K), dtype=torch.uint8, device="cuda")  # aliased by the export, never read
+    comp = mx.export_mxfp8(payload, d, shape=(rows, K), layout="swizzled")
+    small = [(300, 7184), (129, 640)]
+    small_sw = [torch.from_numpy(_random_swizzled(r, k, seed=r + k)).cuda() for r, k in small]
+    grouped = mx.export_mxfp8_grouped(
+        [{"data": torch.empty((r, k), dtype=torch.uint8, device="cuda"), "scales": t, "shape": (r, k),
+          "layout": "swizzled"} for (r, k), t in zip(small, small_sw)] +
+        [{"data": payload, "scales": d, "shape": (rows, K), "layout": "swizzled"}])
+    torch.cuda.synchronize()
+    assert torch.equal(grouped[2].scale_inv, comp.scale_inv)
+    tile = oracle.scale_bytes(128, K, oracle.SWIZZLED)
+    got = host_bits(comp.scale_inv).reshape(rows, nb)
+    for t in (0, 1, 40000, 65535, 65536):
+        want = oracle.export_scales(sw[t * tile:(t + 1) * tile], oracle.SWIZZLED, 128, K)
+        np.testing.assert_array_equal(got[t * 128:(t + 1) * 128], want)
+    for (r, k), t, c in zip(small, small_sw, grouped[:2]):
+        np.testing.assert_array_equal(host_bits(c.scale_inv).reshape(r, -1),
+                                      oracle.export_scales(host_bits(t), oracle.SWIZZLED, r, k))
 
 
 def test_grouped_export_matches_single_exports(mx):
