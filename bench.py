@@ -4,10 +4,12 @@ One step = the whole hot path once: MXFP4 projection, direct MXFP8 rowwise
 (GEMM-swizzled scales), direct FP8 128x128 blockwise, dequantize (MXFP8
 rowwise -> bf16) and export_components (swizzled -> compact scales), each a
 single libmxq kernel.  Throughput is the algorithmic bytes of the five
-conversions over the step time, in GB/s; each conversion is also reported
-against the measured HBM copy bandwidth.
+conversions over the step time, in GB/s; each conversion (and every other
+entry point of the library) is also timed alone and reported against the
+measured HBM copy bandwidth.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxq|reference]
+    python bench.py --profile NAME    # one conversion, 3 launches, small footprint (for ncu)
 
 ``--impl reference`` times the CPU oracle (the only reference this method
 has) on a bounded sample of the same workload.  Under torchrun every rank
@@ -17,12 +19,16 @@ converts its own weight (weak scaling, no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
+import math
 import os
+import signal
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -47,6 +53,18 @@ BYTES = {
     "dequant_bf16": N + N // 32 + 2 * N,
     "export": 2 * (ROWS * NB),
 }
+STEP_BYTES = sum(BYTES.values())
+# The library's other entry points on the same weight, timed alone the same way.
+EXTRA_BYTES = {
+    "mxfp8_col": 2 * N + N + N // 32,
+    "mxfp8_col_dequant_bf16": N + N // 32 + 2 * N,
+    "mxfp4_pack": 2 * N + N // 2 + N // 32,
+    "mxfp4_dequant_bf16": N // 2 + N // 32 + 2 * N,
+    "dequant_fp32": N + N // 32 + 4 * N,
+    "dequant_block128_bf16": N + 4 * TILES + 2 * N,
+    "dequant_block128_fp32": N + 4 * TILES + 4 * N,
+    "quantize_export": 2 * N + N + N // 32,
+}
 KERNEL_FILES = {
     "projection": "mxq_rowwise.cu",
     "mxfp8_row": "mxq_rowwise.cu",
@@ -54,19 +72,20 @@ KERNEL_FILES = {
     "dequant_bf16": "mxq_dequant.cu",
     "export": "mxq_export.cu",
     "mxfp8_col": "mxq_colwise.cu",
+    "mxfp8_col_dequant_bf16": "mxq_colwise.cu",
     "mxfp4_pack": "mxq_rowwise.cu",
     "mxfp4_dequant_bf16": "mxq_dequant.cu",
-    "mxfp8_col_dequant_bf16": "mxq_colwise.cu",
-}
-STEP_BYTES = sum(BYTES.values())
-# Conversions beyond the five of the step, timed alone the same way.
-EXTRA_BYTES = {
-    "mxfp8_col": 2 * N + N + N // 32,
-    "mxfp4_pack": 2 * N + N // 2 + N // 32,
-    "mxfp4_dequant_bf16": N // 2 + N // 32 + 2 * N,
-    "mxfp8_col_dequant_bf16": N + N // 32 + 2 * N,
+    "dequant_fp32": "mxq_dequant.cu",
+    "dequant_block128_bf16": "mxq_dequant.cu",
+    "dequant_block128_fp32": "mxq_dequant.cu",
+    "quantize_export": "mxq_rowwise.cu",
+    "moe_export": "mxq_export.cu",
+    "moe_grouped_export": "mxq_export.cu",
 }
 CSRC = os.path.join(ROOT, "block_scaled_precision_x32_gb300", "csrc")
+# Launches per timed replay of one conversion: the inputs rotate over their
+# resident copies LOOPS times, so the first launch's ramp is a small share.
+LOOPS = 4
 
 
 def kernel_source_hash(name: str) -> str:
@@ -87,7 +106,7 @@ def load_peaks():
 
 
 def load_traffic():
-    """Per-kernel DRAM bytes per launch from the committed ncu summary, kept
+    """Per-kernel traffic per launch from the committed ncu summary, kept
     only while the kernel's sources are unchanged since the capture."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
@@ -97,53 +116,230 @@ def load_traffic():
     out = {}
     for name, rec in d.get("kernels", {}).items():
         if name in KERNEL_FILES and rec.get("source_hash") == kernel_source_hash(name):
-            out[name] = rec.get("dram_bytes_per_launch")
+            out[name] = rec
     return out
 
 
-class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons every 100 ms
+    over the whole GPU section.  Each sample carries nvidia-smi's own
+    timestamp, so the samples inside each timed region (host wall times
+    taken after synchronizing on both sides) are picked out afterwards."""
 
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
+    def __init__(self, index: int, period_ms: int = 100):
+        self.index, self.period_ms = index, period_ms
+        self.samples = []  # (wall time, sm MHz, max sm MHz, power W, set of active reasons)
+        self.regions = {}
+        self.proc = self.thread = None
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True,
+                bufsize=1)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
         return self
 
-    def __exit__(self, *exc):
-        if self.proc is None:
-            self.result = None
-            return
-        self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+    def _read(self):
+        for line in self.proc.stdout:
+            arrived = time.time()
             f = [c.strip() for c in line.split(",")]
-            if len(f) < 7:
+            if len(f) < 8:
                 continue
             try:
-                sm.append(float(f[0]))
-                mx = max(mx, float(f[1]))
+                t = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                t = arrived
+            try:
+                sm, mx = float(f[1]), float(f[2])
             except ValueError:
                 continue
-            for nm, v in zip(names, f[3:7]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        self.result = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
-                       "reasons": sorted(reasons), "samples": len(sm)}
+            try:
+                pw = float(f[3])
+            except ValueError:
+                pw = None
+            self.samples.append((t, sm, mx, pw, {nm for nm, v in zip(self.NAMES, f[4:8]) if v.lower() == "active"}))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.send_signal(signal.SIGINT)
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait(timeout=5)
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def mark(self, name: str, t0: float, t1: float):
+        self.regions[name] = (t0, t1)
+
+    def summary(self, names=None):
+        """Median SM clock, max clock, throttle reasons of the samples that
+        fall inside the named regions (all regions by default)."""
+        if self.proc is None:
+            return None
+        regs = [self.regions[n] for n in (self.regions if names is None else names) if n in self.regions]
+        sel = [s for s in self.samples if any(a <= s[0] <= b for a, b in regs)]
+        reasons = set()
+        for s in sel:
+            reasons |= s[4]
+        pw = [s[3] for s in sel if s[3] is not None]
+        return {"sm_mhz": statistics.median([s[1] for s in sel]) if sel else None,
+                "sm_max_mhz": max((s[2] for s in self.samples), default=None),
+                "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(sel), "samples_total": len(self.samples)}
+
+
+# ---------------------------------------------------------------- timing
+
+def sync():
+    import torch
+
+    torch.cuda.synchronize()
+
+
+def time_replays(g, per_replay: int, stream, world, clocks=None, name=None, min_reps: int = 50,
+                 min_s: float = 0.3, max_reps: int = 20000):
+    """Event-time each replay of CUDA graph g (per_replay launches of one
+    conversion) on its own: at least min_reps replays and about min_s
+    seconds of them.  Returns (median ms per launch, mean ms per launch,
+    replays) -- the max over ranks of each."""
+    import torch
+
+    g.replay()
+    sync()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(5):
+        g.replay()
+    b.record(stream)
+    sync()
+    est = max(a.elapsed_time(b) / 5, 1e-4)
+    n = int(min(max_reps, max(min_reps, math.ceil(min_s * 1e3 / est))))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    barrier(world)
+    sync()
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(2_000_000)  # ~1 ms of GPU time: the host gets ahead before the first event
+    t0 = time.time()
+    for ea, eb in evs:
+        ea.record(stream)
+        g.replay()
+        eb.record(stream)
+    sync()
+    t1 = time.time()
+    if clocks is not None and name is not None:
+        clocks.mark(name, t0, t1)
+    ts = [ea.elapsed_time(eb) / per_replay for ea, eb in evs]
+    return max_over_ranks(statistics.median(ts), world), max_over_ranks(statistics.fmean(ts), world), n
+
+
+class RawGraph:
+    """A CUDA graph of prepared libmxq calls, captured and launched through
+    the CUDA runtime API itself.  (torch's CUDAGraph.replay() also refills its
+    random-generator seed and offset tensors -- two small kernels per replay
+    -- which would sit inside the timed regions.)  replay() launches on the
+    current torch stream."""
+
+    _rt = None
+
+    @classmethod
+    def runtime(cls):
+        if cls._rt is None:
+            import ctypes
+            import glob
+
+            import torch
+
+            cands = [os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64", "libcudart.so")]
+            cands += sorted(glob.glob(os.path.join(os.path.dirname(os.path.dirname(torch.__file__)), "nvidia", "*",
+                                                   "lib", "libcudart.so*")))
+            cands += ["libcudart.so", "libcudart.so.13"]
+            err = None
+            for c in cands:
+                try:
+                    rt = ctypes.CDLL(c)
+                    break
+                except OSError as e:
+                    err = e
+            else:
+                raise RuntimeError(f"libcudart not found: {err}")
+            vp = ctypes.c_void_p
+            rt.cudaStreamBeginCapture.argtypes = [vp, ctypes.c_int]
+            rt.cudaStreamEndCapture.argtypes = [vp, ctypes.POINTER(vp)]
+            rt.cudaGraphInstantiate.argtypes = [ctypes.POINTER(vp), vp, ctypes.c_ulonglong]
+            rt.cudaGraphLaunch.argtypes = [vp, vp]
+            rt.cudaGraphExecDestroy.argtypes = [vp]
+            rt.cudaGraphDestroy.argtypes = [vp]
+            cls._rt = rt
+        return cls._rt
+
+    def __init__(self, calls, stream):
+        import ctypes
+
+        rt = self.runtime()
+        h = ctypes.c_void_p(stream.cuda_stream)
+
+        def ok(code, what):
+            if code != 0:
+                raise RuntimeError(f"{what} failed with CUDA error {code}")
+
+        ok(rt.cudaStreamBeginCapture(h, 0), "cudaStreamBeginCapture")  # global capture mode
+        try:
+            for c in calls:
+                c()
+        finally:
+            self.graph = ctypes.c_void_p()
+            ok(rt.cudaStreamEndCapture(h, ctypes.byref(self.graph)), "cudaStreamEndCapture")
+        self.exe = ctypes.c_void_p()
+        ok(rt.cudaGraphInstantiate(ctypes.byref(self.exe), self.graph, 0), "cudaGraphInstantiate")
+        self._ok = ok
+
+    def replay(self):
+        import ctypes
+
+        import torch
+
+        self._ok(self.runtime().cudaGraphLaunch(self.exe, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)),
+                 "cudaGraphLaunch")
+
+    def __del__(self):
+        rt = self._rt
+        if rt is not None and getattr(self, "exe", None):
+            rt.cudaGraphExecDestroy(self.exe)
+            rt.cudaGraphDestroy(self.graph)
+
+
+def capture(calls, stream):
+    """One CUDA graph holding the given prepared calls, in order."""
+    return RawGraph(calls, stream)
+
+
+def record(name, nbytes, med_ms, mean_ms, reps, peak, clocks, in_step=None):
+    us = med_ms * 1e3
+    gbs = nbytes / (us * 1e-6) / 1e9
+    rec = {"us": round(us, 2), "us_mean": round(mean_ms * 1e3, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+           "bytes": nbytes, "replays": reps}
+    if in_step is not None:
+        rec["in_step"] = in_step
+    c = clocks.summary([name]) if clocks is not None else None
+    if c and c["sm_mhz"]:
+        rec["sm_mhz"] = c["sm_mhz"]
+        rec["clock_samples"] = c["samples"]
+        rec["sm_kcycles"] = round(us * c["sm_mhz"] / 1e3, 2)  # us x MHz / 1000: thousands of SM cycles
+    return rec
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -158,6 +354,7 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(dev)
     lib = mxq.library()
     stream = torch.cuda.current_stream(dev)
+    peak, peak_src = load_peaks()
 
     x_host = syn.normal_bf16(ROWS, COLS, seed=syn.SEED_BASE + 3 + 100 * rank)
     x0 = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -168,28 +365,27 @@ def run_gpu(args, rank, world):
     row_s = torch.empty(lib.scale_bytes(ROWS, COLS, "swizzled"), dtype=torch.uint8, device=dev)
     blk_d = torch.empty_like(row_d)
     blk_s = torch.empty(lib.tile_scale_count(ROWS, COLS), dtype=torch.float32, device=dev)
-    dq_in = []
-    for i in range(R):
-        d, s = lib.mxfp8_row_direct(xs[i], "swizzled")
-        dq_in.append((d, s))
+    dq_in = [lib.mxfp8_row_direct(xs[i], "swizzled") for i in range(R)]
+    blk_in = [lib.fp8_block128_direct(xs[i]) for i in range(R)]
     dq_out = torch.empty_like(x0)
+    dq_out32 = torch.empty((ROWS, COLS), dtype=torch.float32, device=dev)
     ex_out = torch.empty(ROWS * NB, dtype=torch.uint8, device=dev)
     p4 = torch.empty((ROWS, COLS // 2), dtype=torch.uint8, device=dev)
     p4_s = torch.empty(lib.scale_bytes(ROWS, COLS, "swizzled"), dtype=torch.uint8, device=dev)
     p4_in = [lib.mxfp4_pack(xs[i], "swizzled") for i in range(R)]
-    p4_out = torch.empty_like(x0)
     col_in = [lib.mxfp8_col_direct(xs[i], "swizzled") for i in range(R)]
-    col_out = torch.empty_like(x0)
     col_d = torch.empty_like(row_d)
     col_s = torch.empty(lib.scale_bytes(COLS, ROWS, "swizzled"), dtype=torch.uint8, device=dev)
-    torch.cuda.synchronize()
+    qe_s = torch.empty((ROWS, NB), dtype=torch.uint8, device=dev)
+    sync()
 
     names = list(BYTES)
     extra = list(EXTRA_BYTES)
     # Prepared calls (arguments marshalled once), made on a side stream and
     # captured into CUDA graphs: one graph per input rotation holding the
     # step's five launches, and per conversion one graph of R back-to-back
-    # launches.  Replays leave the host out of the timed loop.
+    # launches over the R input copies.  Replays keep the host out of the
+    # timed loop.
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(side):
@@ -204,92 +400,74 @@ def run_gpu(args, rank, world):
                 lib.plan_dequantize(dq_d, dq_out, scales=dq_s, layout="swizzled"),
                 lib.plan_export_mxfp8(dq_d, dq_s, shape=(ROWS, COLS), layout="swizzled", scale_out=ex_out)[0],
             ])
-        extra_plans = [[lib.plan_mxfp8_col_direct(xs[s], "swizzled", col_d, col_s),
-                        lib.plan_mxfp4_pack(xs[s], "swizzled", p4, p4_s),
-                        lib.plan_dequantize(p4_in[s][0], p4_out, scales=p4_in[s][1], layout="swizzled", mxfp4=True),
-                        lib.plan_dequantize(col_in[s][0], col_out, scales=col_in[s][1], layout="swizzled",
-                                            columnwise=True)]
-                       for s in range(R)]
+        extra_plans = [{
+            "mxfp8_col": lib.plan_mxfp8_col_direct(xs[s], "swizzled", col_d, col_s),
+            "mxfp8_col_dequant_bf16": lib.plan_dequantize(col_in[s][0], dq_out, scales=col_in[s][1],
+                                                          layout="swizzled", columnwise=True),
+            "mxfp4_pack": lib.plan_mxfp4_pack(xs[s], "swizzled", p4, p4_s),
+            "mxfp4_dequant_bf16": lib.plan_dequantize(p4_in[s][0], dq_out, scales=p4_in[s][1], layout="swizzled",
+                                                      mxfp4=True),
+            "dequant_fp32": lib.plan_dequantize(dq_in[s][0], dq_out32, scales=dq_in[s][1], layout="swizzled"),
+            "dequant_block128_bf16": lib.plan_dequantize(blk_in[s][0], dq_out, tile_scale_inv=blk_in[s][1]),
+            "dequant_block128_fp32": lib.plan_dequantize(blk_in[s][0], dq_out32, tile_scale_inv=blk_in[s][1]),
+            "quantize_export": lib.plan_quantize_export_mxfp8(xs[s], row_d, qe_s)[0],
+        } for s in range(R)]
         for s in range(2 * R):  # warm every launch configuration before capture
-            for c in plans[s % R] + extra_plans[s % R]:
+            for c in plans[s % R] + list(extra_plans[s % R].values()):
                 c()
         side.synchronize()
-        step_graphs, conv_graphs = [], []
-        for s in range(R):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=side):
-                for c in plans[s]:
-                    c()
-            step_graphs.append(g)
-        for i in range(len(names)):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=side):
-                for s in range(R):
-                    plans[s][i]()
-            conv_graphs.append(g)
-        for i in range(len(extra)):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=side):
-                for s in range(R):
-                    extra_plans[s][i]()
-            conv_graphs.append(g)
+        step_graphs = [capture(plans[s], side) for s in range(R)]
+        conv_graphs = {nm: capture([plans[s][i] for s in range(R)] * LOOPS, side) for i, nm in enumerate(names)}
+        for nm in extra:
+            conv_graphs[nm] = capture([extra_plans[s][nm] for s in range(R)] * LOOPS, side)
     torch.cuda.current_stream(dev).wait_stream(side)
-    torch.cuda.synchronize()
+    sync()
 
+    clocks = ClockSampler(dev.index).start()
+    time.sleep(0.3)  # the sampler's first lines
     for s in range(args.warmup):
         step_graphs[s % R].replay()
-    torch.cuda.synchronize()
+    sync()
 
     # timed region 1: exactly `steps` steps
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    torch.cuda.synchronize()
-    with Clocks(dev.index) as clk:
-        t0.record(stream)
-        for s in range(args.steps):
-            step_graphs[s % R].replay()
-        t1.record(stream)
-        torch.cuda.synchronize()
+    sync()
+    w0 = time.time()
+    t0.record(stream)
+    for s in range(args.steps):
+        step_graphs[s % R].replay()
+    t1.record(stream)
+    sync()
+    clocks.mark("step", w0, time.time())
     barrier(world)
     elapsed_ms = t0.elapsed_time(t1)
     ms_step = max_over_ranks(elapsed_ms, world) / args.steps
 
-    # timed region 2: each conversion alone, R * ceil(steps / R) launches back to back
-    reps = max(1, -(-args.steps // R))
-    per = {}
-    for i, nm in enumerate(names + extra):
-        conv_graphs[i].replay()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record(stream)
-        for _ in range(reps):
-            conv_graphs[i].replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        per[nm] = max_over_ranks(a.elapsed_time(b), world) / (reps * R)
+    # timed region 2: each conversion alone, >= 50 individually timed replays
+    # of R * LOOPS back-to-back launches and >= 0.3 s of them; the median is reported
+    per_conv = {}
+    for nm in names + extra:
+        med, mean, n = time_replays(conv_graphs[nm], R * LOOPS, stream, world, clocks, nm)
+        per_conv[nm] = record(nm, BYTES.get(nm, EXTRA_BYTES.get(nm)), med, mean, n, peak, clocks, nm in BYTES)
+    del conv_graphs, step_graphs
+
+    # the MoE expert stack: MXFP8 rowwise into swizzled scales, then export to compact
+    moe = None if args.no_moe else run_moe(args, lib, dev, stream, world, clocks, peak)
+
+    # the same conversions of an fp32 weight (fp32 master weights)
+    fp32 = None if args.no_fp32 else run_fp32(args, lib, dev, stream, world, clocks, peak)
+    clocks.stop()
 
     # end to end through the public API: pinned host weight in, every result back to pinned host memory
     e2e = None if args.no_e2e else run_e2e(args, lib, dev, x_host, world)
 
-    # the MoE expert stack: MXFP8 rowwise into swizzled scales, then export to compact
-    moe = None if args.no_moe else run_moe(args, lib, dev, stream, world)
-
-    # the same conversions of an fp32 weight (fp32 master weights)
-    fp32 = None if args.no_fp32 else run_fp32(args, lib, dev, stream, world)
-
     if rank != 0:
         return None
-    peak, peak_src = load_peaks()
-    per_conv = {}
-    for nm in names + extra:
-        nbytes = BYTES.get(nm, EXTRA_BYTES.get(nm))
-        us = per[nm] * 1e3
-        gbs = nbytes / (us * 1e-6) / 1e9
-        per_conv[nm] = {"us": round(us, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nbytes,
-                        "in_step": nm in BYTES}
     dom = max(names, key=lambda nm: per_conv[nm]["us"])
-    traffic = load_traffic()
+    traffic = load_traffic().get(dom, {})
     value = world * STEP_BYTES / (ms_step * 1e-3) / 1e9
+    clk = clocks.summary()
     return {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -301,25 +479,30 @@ def run_gpu(args, rank, world):
         "per_conversion": per_conv,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": per_conv[dom]["GBps"], "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src,
-                     "unit": "GB/s", "frac": per_conv[dom]["frac"], "traffic": traffic.get(dom),
-                     "algorithmic_bytes": BYTES[dom]},
-        "clocks": clk.result,
+                     "unit": "GB/s", "frac": per_conv[dom]["frac"], "traffic": traffic.get("traffic"),
+                     "traffic_def": traffic.get("traffic_def"),
+                     "dram_read": traffic.get("dram_read"), "dram_write": traffic.get("dram_write"),
+                     "l2_write": traffic.get("l2_write"), "algorithmic_bytes": BYTES[dom]},
+        "clocks": clk,
         "e2e": e2e,
         "moe": moe,
         "fp32": fp32,
         "gpu_launches": len(names) * args.steps,
         "timing": "CUDA events on the launch stream; steps replay one CUDA graph per input rotation (5 launches "
-                  "each); per_conversion replays per-kernel graphs of back-to-back launches",
+                  "each); per_conversion: median over >= 50 individually event-timed replays (>= 0.3 s) of a graph "
+                  "of 16 back-to-back launches over 4 rotating inputs (MoE: 16 over 8, fp32: 12 over 3); clocks: "
+                  "nvidia-smi samples inside the timed regions",
     }
 
 
-def run_moe(args, lib, dev, stream, world):
+def run_moe(args, lib, dev, stream, world, clocks, peak):
     """32 experts x 4096 x 7184 bf16 (K % 32 = 16: 225 scale columns, padded
     to 228), each expert N(0, 0.02) * 2^U{-8..8} from its own seed.  Times
     the MXFP8 rowwise conversion of the whole stack into GEMM-swizzled scales
-    (one launch, 2.8 GB of traffic, larger than L2) and the export of those
+    (one launch, 2.8 GB of traffic, larger than L2), the export of those
     scales to compact (8 rotating copies of the 29.9 MB swizzled buffer, so
-    reads come from HBM)."""
+    reads come from HBM), and the same export with the 32 experts as
+    separate storages (the grouped export, one launch per copy)."""
     import concurrent.futures as cf
 
     import torch
@@ -333,12 +516,11 @@ def run_moe(args, lib, dev, stream, world):
         for e, h in enumerate(ex.map(syn.moe_expert_bf16, range(E))):
             x[e].copy_(torch.from_numpy(h.view(np.int16)).view(torch.bfloat16))
     sbytes = lib.scale_bytes(rows, K, "swizzled")
+    per_expert = lib.scale_bytes(Rw, K, "swizzled")
     data = torch.empty((E, Rw, K), dtype=torch.uint8, device=dev)
     R = 8
     sw = [torch.empty(sbytes, dtype=torch.uint8, device=dev) for _ in range(R)]
     out = torch.empty(rows * nb, dtype=torch.uint8, device=dev)
-    # prepared calls captured into CUDA graphs (as for the 8192 x 8192 step), so
-    # host launch overhead stays out of the timed loop
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(side):
@@ -348,55 +530,33 @@ def run_moe(args, lib, dev, stream, world):
             sw[i].copy_(sw[0])
         exports = [lib.plan_export_mxfp8(data, sw[i], shape=(E, Rw, K), layout="swizzled", scale_out=out)[0]
                    for i in range(R)]
-        for c in exports:
+        grouped = [lib.plan_export_mxfp8_grouped(
+            [{"data": data[e], "scales": sw[i][e * per_expert:(e + 1) * per_expert], "shape": (Rw, K),
+              "layout": "swizzled"} for e in range(E)], scale_out=out)[0] for i in range(R)]
+        for c in exports + grouped:
             c()
         side.synchronize()
-        g_row, g_ex = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_row, stream=side):
-            row()
-        with torch.cuda.graph(g_ex, stream=side):
-            for c in exports:
-                c()
+        g_row, g_ex, g_grp = capture([row], side), capture(exports * 2, side), capture(grouped * 2, side)
     torch.cuda.current_stream(dev).wait_stream(side)
-    torch.cuda.synchronize()
-    g_row.replay()
-    g_ex.replay()
-    torch.cuda.synchronize()
-
-    def timed(fn, reps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record(stream)
-        for _ in range(reps):
-            fn()
-        b.record(stream)
-        torch.cuda.synchronize()
-        return max_over_ranks(a.elapsed_time(b), world) / reps
-
-    row_reps = max(3, min(50, args.steps // 40))
-    ex_reps = max(1, min(200, args.steps // 10))
-    row_ms = timed(g_row.replay, row_reps)
-    ex_ms = timed(g_ex.replay, ex_reps) / R
-    peak, _ = load_peaks()
+    sync()
     row_bytes = 3 * rows * K + sbytes
     ex_bytes = sbytes + rows * nb
-    del x, data, sw, g_row, g_ex
+    res = {"workload": f"MoE expert stack {E}x{Rw}x{K} bf16, N(0,0.02)*2^U{{-8..8}} per expert (synthetic)"}
+    for nm, g, per, nbytes in (("moe_mxfp8_row", g_row, 1, row_bytes), ("moe_export", g_ex, 2 * R, ex_bytes),
+                               ("moe_grouped_export", g_grp, 2 * R, ex_bytes)):
+        med, mean, n = time_replays(g, per, stream, world, clocks, nm)
+        res[{"moe_mxfp8_row": "mxfp8_row_swizzled", "moe_export": "export_swizzled_to_compact",
+             "moe_grouped_export": "grouped_export_32_storages"}[nm]] = record(nm, nbytes, med, mean, n, peak, clocks)
+    del x, data, sw, g_row, g_ex, g_grp
     torch.cuda.empty_cache()
-
-    def rec(ms, nbytes):
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        return {"us": round(ms * 1e3, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nbytes}
-
-    return {"workload": f"MoE expert stack {E}x{Rw}x{K} bf16, N(0,0.02)*2^U{{-8..8}} per expert (synthetic)",
-            "mxfp8_row_swizzled": rec(row_ms, row_bytes), "export_swizzled_to_compact": rec(ex_ms, ex_bytes),
-            "reps": {"mxfp8_row": row_reps, "export": ex_reps * R}}
+    return res
 
 
-def run_fp32(args, lib, dev, stream, world):
+def run_fp32(args, lib, dev, stream, world, clocks, peak):
     """The step's conversions and the columnwise / packed forms of an
     8192 x 8192 fp32 weight (N(0, 0.02), seed 1003), three rotating copies
     (800 MB, beyond L2), each conversion a CUDA graph of back-to-back
-    launches timed with events."""
+    launches timed as the bf16 conversions are."""
     import torch
 
     from block_scaled_precision_x32_gb300 import synthetic as syn
@@ -418,7 +578,7 @@ def run_fp32(args, lib, dev, stream, world):
     conv = {
         "projection": (lambda x: lib.plan_fake_quant_mxfp4(x, y), 8 * N),
         "mxfp8_row": (lambda x: lib.plan_mxfp8_row_direct(x, "swizzled", rd, rs), 5 * N + N // 32),
-        "block128": (lambda x: lib.plan_fp8_block128_direct(x, bd, bs), 5 * N + 4 * (ROWS // 128) * (COLS // 128)),
+        "block128": (lambda x: lib.plan_fp8_block128_direct(x, bd, bs), 5 * N + 4 * TILES),
         "mxfp8_col": (lambda x: lib.plan_mxfp8_col_direct(x, "swizzled", cd, cs), 5 * N + N // 32),
         "mxfp4_pack": (lambda x: lib.plan_mxfp4_pack(x, "swizzled", pk, ps), 4 * N + N // 2 + N // 32),
     }
@@ -431,28 +591,13 @@ def run_fp32(args, lib, dev, stream, world):
             for c in calls:
                 c()
             side.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=side):
-                for c in calls:
-                    c()
-            graphs[nm] = (g, nbytes)
+            graphs[nm] = (capture(calls * LOOPS, side), nbytes)
     torch.cuda.current_stream(dev).wait_stream(side)
-    torch.cuda.synchronize()
-    peak, _ = load_peaks()
-    reps = max(3, min(100, args.steps // 20))
+    sync()
     out = {"workload": "8192x8192 fp32 weight (the bench weight widened), 3 rotating copies"}
     for nm, (g, nbytes) in graphs.items():
-        g.replay()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record(stream)
-        for _ in range(reps):
-            g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = max_over_ranks(a.elapsed_time(b), world) / (reps * R)
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        out[nm] = {"us": round(ms * 1e3, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nbytes}
+        med, mean, n = time_replays(g, R * LOOPS, stream, world, clocks, "fp32_" + nm)
+        out[nm] = record("fp32_" + nm, nbytes, med, mean, n, peak, clocks)
     del xs, graphs
     torch.cuda.empty_cache()
     return out
@@ -533,11 +678,11 @@ def run_e2e(args, lib, dev, x_host, world, chunks: int = 2):
     main = torch.cuda.current_stream(dev)
     for _ in range(max(1, args.warmup)):
         step()
-    torch.cuda.synchronize()
+    sync()
     n = max(1, min(args.steps, 10))
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    torch.cuda.synchronize()
+    sync()
     t0.record(main)
     for st in (s_in, s_cmp, s_out):
         st.wait_event(t0)
@@ -546,7 +691,7 @@ def run_e2e(args, lib, dev, x_host, world, chunks: int = 2):
     for st in (s_in, s_cmp, s_out):
         main.wait_stream(st)
     t1.record(main)
-    torch.cuda.synchronize()
+    sync()
     ms = max_over_ranks(t0.elapsed_time(t1), world) / n
     d2h = sum(t.numel() * t.element_size() for t in host.values())
     return {"value": round(world * STEP_BYTES / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 3),
@@ -554,16 +699,112 @@ def run_e2e(args, lib, dev, x_host, world, chunks: int = 2):
             "pipeline": f"{chunks} row chunks over 3 streams (upload / convert / download)"}
 
 
+# ------------------------------------------------- small driver for ncu
+
+PROFILE_NAMES = ("projection", "mxfp8_row", "block128", "dequant_bf16", "export", "mxfp8_col",
+                 "mxfp8_col_dequant_bf16", "mxfp4_pack", "mxfp4_dequant_bf16", "dequant_fp32",
+                 "dequant_block128_bf16", "quantize_export", "fp32_block128", "fp32_mxfp8_col", "moe_export",
+                 "moe_grouped_export")
+
+
+def run_profile(name: str, reps: int = 3):
+    """One conversion of the benchmark, `reps` launches, with only the
+    buffers it needs (at most about 1 GB on the device), for ncu captures of
+    a single kernel.  The 8192 x 8192 weight (134 MB bf16, 268 MB fp32) is
+    larger than L2.  The MoE exports take a 29.9 MB swizzled scale buffer
+    of the expert stack's shape filled with random bytes (the copy moves
+    bytes; their values do not change its work) and an uninitialised
+    payload for the export to alias, without the 1.9 GB bf16 stack.
+    Inputs of the timed kernel are produced first by other kernels."""
+    import torch
+
+    import block_scaled_precision_x32_gb300 as mxq
+    from block_scaled_precision_x32_gb300 import synthetic as syn
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib = mxq.library()
+    if name.startswith("moe_"):
+        E, Rw, K = syn.MOE_EXPERTS, syn.MOE_ROWS, syn.MOE_K
+        rows, nb = E * Rw, -(-K // 32)
+        g = torch.Generator(device=dev)
+        g.manual_seed(1005)
+        sw = torch.randint(0, 256, (lib.scale_bytes(rows, K, "swizzled"),), dtype=torch.uint8, device=dev,
+                           generator=g)
+        # the payload an export aliases (its bytes are never read: left uninitialised)
+        data = torch.empty((E, Rw, K), dtype=torch.uint8, device=dev)
+        out = torch.empty(rows * nb, dtype=torch.uint8, device=dev)
+        if name == "moe_export":
+            call = lib.plan_export_mxfp8(data, sw, shape=(E, Rw, K), layout="swizzled", scale_out=out)[0]
+        else:
+            pe = lib.scale_bytes(Rw, K, "swizzled")
+            call = lib.plan_export_mxfp8_grouped(
+                [{"data": data[e], "scales": sw[e * pe:(e + 1) * pe], "shape": (Rw, K), "layout": "swizzled"}
+                 for e in range(E)], scale_out=out)[0]
+    else:
+        x = torch.from_numpy(syn.normal_bf16(ROWS, COLS).view(np.int16)).view(torch.bfloat16).to(dev)
+        if name.startswith("fp32_"):
+            x = x.float()
+        u8 = lambda *s: torch.empty(s, dtype=torch.uint8, device=dev)  # noqa: E731
+        if name == "projection":
+            call = lib.plan_fake_quant_mxfp4(x, torch.empty_like(x))
+        elif name == "mxfp8_row":
+            call = lib.plan_mxfp8_row_direct(x, "swizzled", u8(ROWS, COLS), u8(lib.scale_bytes(ROWS, COLS, 2)))
+        elif name in ("block128", "fp32_block128"):
+            call = lib.plan_fp8_block128_direct(x, u8(ROWS, COLS), torch.empty(TILES, dtype=torch.float32,
+                                                                               device=dev))
+        elif name in ("mxfp8_col", "fp32_mxfp8_col"):
+            call = lib.plan_mxfp8_col_direct(x, "swizzled", u8(ROWS, COLS), u8(lib.scale_bytes(COLS, ROWS, 2)))
+        elif name == "mxfp4_pack":
+            call = lib.plan_mxfp4_pack(x, "swizzled", u8(ROWS, COLS // 2), u8(lib.scale_bytes(ROWS, COLS, 2)))
+        elif name == "quantize_export":
+            call = lib.plan_quantize_export_mxfp8(x, u8(ROWS, COLS), u8(ROWS, NB))[0]
+        elif name in ("dequant_bf16", "dequant_fp32", "export"):
+            d, s = lib.mxfp8_row_direct(x, "swizzled")
+            del x
+            if name == "export":
+                call = lib.plan_export_mxfp8(d, s, shape=(ROWS, COLS), layout="swizzled", scale_out=u8(ROWS * NB))[0]
+            else:
+                out = torch.empty((ROWS, COLS), dtype=torch.bfloat16 if name == "dequant_bf16" else torch.float32,
+                                  device=dev)
+                call = lib.plan_dequantize(d, out, scales=s, layout="swizzled")
+        elif name == "dequant_block128_bf16":
+            d, s = lib.fp8_block128_direct(x)
+            del x
+            call = lib.plan_dequantize(d, torch.empty((ROWS, COLS), dtype=torch.bfloat16, device=dev),
+                                       tile_scale_inv=s)
+        elif name == "mxfp8_col_dequant_bf16":
+            d, s = lib.mxfp8_col_direct(x, "swizzled")
+            del x
+            call = lib.plan_dequantize(d, torch.empty((ROWS, COLS), dtype=torch.bfloat16, device=dev), scales=s,
+                                       layout="swizzled", columnwise=True)
+        elif name == "mxfp4_dequant_bf16":
+            p, s = lib.mxfp4_pack(x, "swizzled")
+            del x
+            call = lib.plan_dequantize(p, torch.empty((ROWS, COLS), dtype=torch.bfloat16, device=dev), scales=s,
+                                       layout="swizzled", mxfp4=True)
+        else:
+            raise SystemExit(f"unknown --profile {name}; one of {', '.join(PROFILE_NAMES)}")
+    sync()
+    for _ in range(reps):
+        call()
+    sync()
+    print(json.dumps({"profile": name, "launches": reps,
+                      "device_bytes": torch.cuda.max_memory_allocated(dev)}), flush=True)
+
+
 # --------------------------------------------------- CPU oracle (reference)
 
-def oracle_sample(cols: int, rows: int = 128, seed: int = 1003):
+def oracle_sample(cols: int, rows: int = 128, seed: int = 1003, x=None):
     """One pass of the whole path through the CPU oracle on a rows x cols
-    slab (multiples of 128) of the weight.  Returns (seconds, algorithmic
-    bytes of the slab)."""
+    slab (multiples of 128) of the weight, or on the given slab x.  Returns
+    (seconds, algorithmic bytes of the slab)."""
     import oracle
     from block_scaled_precision_x32_gb300 import synthetic as syn
 
-    x = syn.normal_bf16(rows, cols, seed=seed)
+    if x is None:
+        x = syn.normal_bf16(rows, cols, seed=seed)
+    rows, cols = x.shape
     t = time.perf_counter()
     oracle.fake_quant_mxfp4(x)
     d, s = oracle.mxfp8_row_direct(x, oracle.SWIZZLED)
@@ -580,7 +821,7 @@ def _cols_for(budget_s: float) -> int:
     return max(128, min(cols, COLS))
 
 
-def cpu_baseline(budget_s: float = 15.0):
+def cpu_baseline_one_core(budget_s: float = 12.0):
     cols = _cols_for(budget_s)
     tot_t = tot_b = 0.0
     reps = 0
@@ -594,31 +835,33 @@ def cpu_baseline(budget_s: float = 15.0):
                       f"single-threaded C oracle, {tot_t:.1f} s"}
 
 
+def cpu_baseline_full():
+    """The whole 8192 x 8192 step (config: the bench weight, seed 1003)
+    through the unchanged oracle on every host core: 64 slabs of 128 rows
+    over one thread per core (the oracle's C functions run outside the GIL
+    through ctypes).  Throughput = the step's algorithmic bytes / wall time
+    of the conversions (generating the weight is not timed)."""
+    import concurrent.futures as cf
+
+    from block_scaled_precision_x32_gb300 import synthetic as syn
+
+    x = syn.normal_bf16(ROWS, COLS)
+    n = os.cpu_count() or 1
+    oracle_sample(128, x=x[:128, :256])  # load the oracle library before the clock starts
+    t = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        res = list(ex.map(lambda i: oracle_sample(COLS, x=x[128 * i:128 * i + 128]), range(ROWS // 128)))
+    wall = time.perf_counter() - t
+    nbytes = sum(b for _, b in res)
+    return {"value": round(nbytes / wall / 1e9, 5), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"the whole 8192 x 8192 bf16 step (5 conversions, {nbytes / 1e6:.1f} MB) as 64 slabs of 128 "
+                      f"rows over {n} threads (one per host core), the single-threaded C oracle unchanged, "
+                      f"{wall:.1f} s wall"}
+
+
 def _oracle_slab(task):
     cols, seed = task
     return oracle_sample(cols, seed=seed)
-
-
-def cpu_baseline_all_cores(budget_s: float = 10.0):
-    """The same oracle on every host core at once: one process per core
-    (spawned, so no CUDA state is inherited), each converting its own
-    128-row slabs.  Throughput = all slabs' bytes / wall time of the pool's
-    work (pool start-up and imports excluded by a warm-up task per worker)."""
-    import multiprocessing as mp
-
-    n = os.cpu_count() or 1
-    cols = _cols_for(budget_s / 2)
-    ctx = mp.get_context("spawn")
-    with ctx.Pool(n) as pool:
-        pool.map(_oracle_slab, [(128, 5000 + i) for i in range(n)])  # start every worker, load the oracle
-        tasks = [(cols, 1003 + i) for i in range(2 * n)]
-        t = time.perf_counter()
-        res = pool.map(_oracle_slab, tasks, chunksize=1)
-        wall = time.perf_counter() - t
-    nbytes = sum(b for _, b in res)
-    return {"value": round(nbytes / wall / 1e9, 5), "unit": "GB/s", "cores": n, "kind": "oracle",
-            "sample": f"{len(tasks)} slabs of 128 x {cols} of the bf16 weight over {n} processes (one per core), "
-                      f"whole step (5 conversions) each, the single-threaded C oracle unchanged, {wall:.1f} s wall"}
 
 
 def _oracle_moe_slab(task):
@@ -732,7 +975,12 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--no-moe", action="store_true", help="skip the MoE expert-stack measurement")
     ap.add_argument("--no-fp32", action="store_true", help="skip the fp32-weight measurement")
+    ap.add_argument("--profile", choices=PROFILE_NAMES, help="run one conversion 3 times on a small footprint "
+                                                               "(for ncu) and exit")
     args = ap.parse_args(argv)
+    if args.profile:
+        run_profile(args.profile)
+        return 0
     if args.warmup < 3:
         args.warmup = 3
     rank, world = dist_env()
@@ -745,8 +993,8 @@ def main(argv=None):
     res = run_gpu(args, rank, world)
     if res is not None:
         if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline()
-            res["cpu_baseline_all_cores"] = cpu_baseline_all_cores()
+            res["cpu_baseline"] = cpu_baseline_full()
+            res["cpu_baseline_one_core"] = cpu_baseline_one_core()
             if not args.no_moe:
                 res["cpu_baseline_moe"] = cpu_baseline_moe()
         print(json.dumps(res), flush=True)
