@@ -492,12 +492,16 @@ __global__ void __launch_bounds__(kThreads) colwise_dequant_kernel(DequantArgs a
 // as for the rowwise form.  A row chunk with a NaN / Inf payload or a
 // code-255 column, or (fp32 output) a column code below which products
 // leave bf16's normal range, takes the element-wise fp32 path.
-// Registers capped near 48 (10 CTAs per SM): 35.5 us on 8192 x 8192 against
-// 38.3 us at the compiler's 72.
+// Registers capped near 40 (12 CTAs per SM) and two bands per CTA: 33.8 us
+// on 8192 x 8192 bf16 out against 35.6 us at one band and 10 CTAs per SM
+// (38.3 us at the compiler's 72 registers; 14 or more CTAs per SM spill,
+// 48-62 us).  fp32 output, whose staging needs more registers, keeps 10 CTAs
+// per SM.
 constexpr int kDqThreads = 128;
+constexpr int kDqBandsPerCta = 2;
 
 template <bool E5M2, bool BF16OUT>
-__global__ void __launch_bounds__(kDqThreads, 10) colwise_dequant_tile_kernel(DequantArgs a, int64_t bands) {
+__global__ void __launch_bounds__(kDqThreads, BF16OUT ? 12 : 10) colwise_dequant_tile_kernel(DequantArgs a, int64_t bands) {
     // multiplier words of chunk q at 16 q + 4 (q / 2): the four chunks' words
     // read by one warp instruction fall in different banks
     __shared__ __align__(16) uint32_t colmul[64 + 8];
@@ -639,7 +643,8 @@ cudaError_t launch_colwise_dequant(const DequantArgs& a, cudaStream_t s) {
     const int oes = a.out_bf16 ? 2 : 4;
     if (a.K % 32 == 0 && aligned(a.data, 32) && aligned(a.out, 32) && (a.K * oes) % 32 == 0) {
         const int64_t bands = ceil_div(a.rows, 32), gx = ceil_div(a.K, 128);
-        const dim3 grid((unsigned)gx, (unsigned)(bands < 65535 ? bands : 65535));
+        const int64_t gy = ceil_div(bands, kDqBandsPerCta);
+        const dim3 grid((unsigned)gx, (unsigned)(gy < 65535 ? gy : 65535));
         if (e5)
             a.out_bf16 ? colwise_dequant_tile_kernel<true, true><<<grid, kDqThreads, 0, s>>>(a, bands)
                        : colwise_dequant_tile_kernel<true, false><<<grid, kDqThreads, 0, s>>>(a, bands);
