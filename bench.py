@@ -327,6 +327,28 @@ def capture(calls, stream):
     return RawGraph(calls, stream)
 
 
+def capture_parallel(branches, streams, fork):
+    """One CUDA graph whose branches run concurrently: branch i (a list of
+    prepared calls planned on streams[i]) forks from streams[0] and joins it
+    again.  The graph holds no other work than the calls."""
+    import torch
+
+    events = [torch.cuda.Event() for _ in streams]
+
+    def body():
+        fork.record(streams[0])
+        for st in streams[1:]:
+            st.wait_event(fork)
+        for calls in branches:
+            for c in calls:
+                c()
+        for ev, st in zip(events[1:], streams[1:]):
+            ev.record(st)
+            streams[0].wait_event(ev)
+
+    return RawGraph([body], streams[0])
+
+
 def record(name, nbytes, med_ms, mean_ms, reps, peak, clocks, in_step=None):
     us = med_ms * 1e3
     gbs = nbytes / (us * 1e-6) / 1e9
@@ -388,6 +410,28 @@ def run_gpu(args, rank, world):
     # timed loop.
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
+    # the step's five conversions read independent inputs (dequantize and
+    # export take an earlier rotation's MXFP8 form), so the step graph runs
+    # them as concurrent branches, each planned on its own stream
+    branch = [side] + [torch.cuda.Stream(dev) for _ in range(len(BYTES) - 1)]
+    for b in branch[1:]:
+        b.wait_stream(torch.cuda.current_stream(dev))
+    step_plans = []
+    for s in range(R):
+        k = 3 * s
+        dq_d, dq_s = dq_in[s]
+        makers = [
+            lambda: lib.plan_fake_quant_mxfp4(xs[k % R], y),
+            lambda: lib.plan_mxfp8_row_direct(xs[(k + 1) % R], "swizzled", row_d, row_s),
+            lambda: lib.plan_fp8_block128_direct(xs[(k + 2) % R], blk_d, blk_s),
+            lambda: lib.plan_dequantize(dq_d, dq_out, scales=dq_s, layout="swizzled"),
+            lambda: lib.plan_export_mxfp8(dq_d, dq_s, shape=(ROWS, COLS), layout="swizzled", scale_out=ex_out)[0],
+        ]
+        row = []
+        for mk, st in zip(makers, branch):
+            with torch.cuda.stream(st):
+                row.append(mk())
+        step_plans.append(row)
     with torch.cuda.stream(side):
         plans = []
         for s in range(R):
@@ -413,10 +457,12 @@ def run_gpu(args, rank, world):
             "quantize_export": lib.plan_quantize_export_mxfp8(xs[s], row_d, qe_s)[0],
         } for s in range(R)]
         for s in range(2 * R):  # warm every launch configuration before capture
-            for c in plans[s % R] + list(extra_plans[s % R].values()):
+            for c in plans[s % R] + step_plans[s % R] + list(extra_plans[s % R].values()):
                 c()
-        side.synchronize()
-        step_graphs = [capture(plans[s], side) for s in range(R)]
+        for b in branch:
+            b.synchronize()
+        fork = torch.cuda.Event()
+        step_graphs = [capture_parallel([[c] for c in step_plans[s]], branch, fork) for s in range(R)]
         conv_graphs = {nm: capture([plans[s][i] for s in range(R)] * LOOPS, side) for i, nm in enumerate(names)}
         for nm in extra:
             conv_graphs[nm] = capture([extra_plans[s][nm] for s in range(R)] * LOOPS, side)
@@ -488,8 +534,8 @@ def run_gpu(args, rank, world):
         "moe": moe,
         "fp32": fp32,
         "gpu_launches": len(names) * args.steps,
-        "timing": "CUDA events on the launch stream; steps replay one CUDA graph per input rotation (5 launches "
-                  "each); per_conversion: median over >= 50 individually event-timed replays (>= 0.3 s) of a graph "
+        "timing": "CUDA events on the launch stream; steps replay one CUDA graph per input rotation (the 5 "
+                  "launches as concurrent branches: the conversions read independent inputs); per_conversion: median over >= 50 individually event-timed replays (>= 0.3 s) of a graph "
                   "of 16 back-to-back launches over 4 rotating inputs (MoE: 16 over 8, fp32: 12 over 3); clocks: "
                   "nvidia-smi samples inside the timed regions",
     }
