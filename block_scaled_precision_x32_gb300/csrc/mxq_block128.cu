@@ -278,15 +278,28 @@ __global__ void __launch_bounds__(T128<ELT>::NT, ELT == Elt::BF16 ? 4 : 2)
     const int t = threadIdx.x;
     if (a.skip != nullptr && *a.skip != 0) return;  // skip-update request: write nothing
     const int64_t ntiles = tiles_r * tiles_c;
+    // The thread's chunks of any tile: row r0 + RPM m, chunk column c (m = 0 ..
+    // NCH - 1); RPM is even, so the slot's XOR term is the same for every m and
+    // the slot steps by RPM * CPR.  Whole tiles copy without bounds checks.
+    constexpr int NCH = 128 * CPR / P::NT, RPM = P::NT / CPR;
+    static_assert(RPM % 2 == 0, "the XOR term of stage_slot must not depend on m");
+    const int r0 = t / CPR, c = t % CPR;
+    const int slot0 = stage_slot<ELT>(r0, c);
+    const int64_t rel0 = (int64_t)r0 * a.ldx + c * (16 / P::ES), relm = (int64_t)RPM * a.ldx;  // elements
     auto stage = [&](int64_t lin) {
         const int64_t ti = lin / tiles_c, tj = lin - ti * tiles_c;
+        const char* base = static_cast<const char*>(a.x) + (ti * 128 * a.ldx + tj * 128) * P::ES;
+        if (ti * 128 + 128 <= a.rows && tj * 128 + 128 <= a.K) {
 #pragma unroll
-        for (int m = 0; m < 128 * CPR / P::NT; ++m) {
-            const int id = m * P::NT + t, r = id / CPR, c = id % CPR;
-            const int64_t row = ti * 128 + r, col = tj * 128 + c * (16 / P::ES);
-            const bool in = row < a.rows && col < a.K;
-            const char* src = static_cast<const char*>(a.x) + (in ? (row * a.ldx + col) * P::ES : 0);
-            cp_async16(&stile[stage_slot<ELT>(r, c)], src, in ? 16 : 0);
+            for (int m = 0; m < NCH; ++m)
+                cp_async16(&stile[slot0 + m * RPM * CPR], base + (rel0 + m * relm) * P::ES, 16);
+        } else {
+#pragma unroll
+            for (int m = 0; m < NCH; ++m) {
+                const int64_t row = ti * 128 + r0 + RPM * m, col = tj * 128 + c * (16 / P::ES);
+                const bool in = row < a.rows && col < a.K;
+                cp_async16(&stile[slot0 + m * RPM * CPR], in ? base + (rel0 + m * relm) * P::ES : base, in ? 16 : 0);
+            }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
