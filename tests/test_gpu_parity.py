@@ -719,16 +719,81 @@ def test_grouped_export_matches_single_exports(mx):
     assert mx.export_mxfp8_grouped([]) == []
 
 
-def test_quantize_export_one_call(mx):
-    """Quantize a bf16 weight and export it in one call (TE issue #3644,
-    workflow 2): values and compact scales equal the oracle's."""
+def test_grouped_export_past_one_launch(mx):
+    """130 storages -- more than one launch of 128 -- mixing every path of
+    the grouped kernel (chunk-path swizzled, other swizzled, padded copies,
+    compact and padded views, empty storages), each equal to the oracle's
+    export of its random scale bytes, copies packed in order into one
+    scale_out."""
+    g = np.random.default_rng(130)
+    kinds = [(40, 7184, "swizzled"), (129, 160, "swizzled"), (64, 48, "padded"), (33, 96, "compact"),
+             (128, 128, "padded"), (0, 64, "swizzled"), (17, 1056, "swizzled"), (1, 16, "padded")]
+    storages, wants = [], []
+    for i in range(130):
+        rows, K, lay = kinds[i % len(kinds)]
+        rows = rows + (i // len(kinds)) % 3 if rows else 0
+        nbytes = oracle.scale_bytes(rows, K, {"compact": oracle.COMPACT, "padded": oracle.PADDED,
+                                              "swizzled": oracle.SWIZZLED}[lay])
+        sc = g.integers(0, 256, size=max(nbytes, 1), dtype=np.uint8)
+        storages.append({"data": torch.empty((rows, K), dtype=torch.uint8, device="cuda"),
+                         "scales": torch.from_numpy(sc).cuda(), "shape": (rows, K), "layout": lay})
+        code = {"compact": oracle.COMPACT, "padded": oracle.PADDED, "swizzled": oracle.SWIZZLED}[lay]
+        wants.append(oracle.export_scales(sc[:nbytes], code, rows, K) if rows else np.zeros((0, (K + 31) // 32),
+                                                                                          np.uint8))
+    comps = mx.export_mxfp8_grouped(storages)
+    torch.cuda.synchronize()
+    assert len(comps) == 130
+    for i, (c, w) in enumerate(zip(comps, wants)):
+        np.testing.assert_array_equal(host_bits(c.scale_inv).reshape(w.shape), w, err_msg=f"storage {i}")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp32"])
+def test_quantize_export_one_call(mx, dt):
+    """Quantize a bf16 or fp32 weight and export it in one call (TE issue
+    #3644, workflow 2): values and compact scales equal the oracle's."""
     x_np = syn.moe_expert_bf16(3, rows=512)
-    comp = mx.quantize_export_mxfp8(dev_bf16(x_np))
+    if dt == "fp32":
+        x_np = syn.bf16_bits_to_f32(x_np) * np.float32(3.0)  # not bf16-representable everywhere
+    comp = mx.quantize_export_mxfp8(dev_input(x_np))
     torch.cuda.synchronize()
     rd, rs = oracle.mxfp8_row_direct(x_np)
     np.testing.assert_array_equal(host_bits(comp.data), rd)
     np.testing.assert_array_equal(host_bits(comp.scale_inv), rs)
     assert comp.is_view and comp.scale_inv.shape == (512, 225)
+
+
+def test_prepared_exports_replay_in_a_graph(mx):
+    """The prepared grouped export and one-call quantize+export capture into
+    a CUDA graph; replays after the inputs change give the oracle's bytes."""
+    xa, xb = syn.normal_bf16(256, 7184, seed=81), syn.normal_bf16(256, 7184, seed=82)
+    x = dev_bf16(xa)
+    d, s = mx.mxfp8_row_direct(x, "swizzled")
+    out = torch.empty(256 * 225, dtype=torch.uint8, device="cuda")
+    qd = torch.empty((256, 7184), dtype=torch.uint8, device="cuda")
+    qs = torch.empty((256, 225), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        calls = [mx.plan_mxfp8_row_direct(x, "swizzled", d, s),
+                 mx.plan_export_mxfp8_grouped([{"data": d, "scales": s, "shape": (256, 7184), "layout": "swizzled"}],
+                                              scale_out=out)[0],
+                 mx.plan_quantize_export_mxfp8(x, qd, qs)[0]]
+        for c in calls:
+            c()
+        side.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for c in calls:
+                c()
+    torch.cuda.current_stream().wait_stream(side)
+    for xn in (xa, xb):
+        x.copy_(dev_bf16(xn))
+        g.replay()
+        torch.cuda.synchronize()
+        rd, rs = oracle.mxfp8_row_direct(xn)
+        np.testing.assert_array_equal(host_bits(out).reshape(256, 225), rs)
+        np.testing.assert_array_equal(host_bits(qd), rd)
+        np.testing.assert_array_equal(host_bits(qs), rs)
 
 
 # ------------------------------------------------------ skip-update flag
