@@ -58,6 +58,7 @@ STEP_BYTES = sum(BYTES.values())
 EXTRA_BYTES = {
     "mxfp8_col": 2 * N + N + N // 32,
     "mxfp8_col_dequant_bf16": N + N // 32 + 2 * N,
+    "mxfp8_col_dequant_fp32": N + N // 32 + 4 * N,
     "mxfp4_pack": 2 * N + N // 2 + N // 32,
     "mxfp4_dequant_bf16": N // 2 + N // 32 + 2 * N,
     "dequant_fp32": N + N // 32 + 4 * N,
@@ -73,6 +74,7 @@ KERNEL_FILES = {
     "export": "mxq_export.cu",
     "mxfp8_col": "mxq_colwise.cu",
     "mxfp8_col_dequant_bf16": "mxq_colwise.cu",
+    "mxfp8_col_dequant_fp32": "mxq_colwise.cu",
     "mxfp4_pack": "mxq_rowwise.cu",
     "mxfp4_dequant_bf16": "mxq_dequant.cu",
     "dequant_fp32": "mxq_dequant.cu",
@@ -448,6 +450,8 @@ def run_gpu(args, rank, world):
             "mxfp8_col": lib.plan_mxfp8_col_direct(xs[s], "swizzled", col_d, col_s),
             "mxfp8_col_dequant_bf16": lib.plan_dequantize(col_in[s][0], dq_out, scales=col_in[s][1],
                                                           layout="swizzled", columnwise=True),
+            "mxfp8_col_dequant_fp32": lib.plan_dequantize(col_in[s][0], dq_out32, scales=col_in[s][1],
+                                                          layout="swizzled", columnwise=True),
             "mxfp4_pack": lib.plan_mxfp4_pack(xs[s], "swizzled", p4, p4_s),
             "mxfp4_dequant_bf16": lib.plan_dequantize(p4_in[s][0], dq_out, scales=p4_in[s][1], layout="swizzled",
                                                       mxfp4=True),
@@ -748,7 +752,7 @@ def run_e2e(args, lib, dev, x_host, world, chunks: int = 2):
 # ------------------------------------------------- small driver for ncu
 
 PROFILE_NAMES = ("projection", "mxfp8_row", "block128", "dequant_bf16", "export", "mxfp8_col",
-                 "mxfp8_col_dequant_bf16", "mxfp4_pack", "mxfp4_dequant_bf16", "dequant_fp32",
+                 "mxfp8_col_dequant_bf16", "mxfp8_col_dequant_fp32", "mxfp4_pack", "mxfp4_dequant_bf16", "dequant_fp32",
                  "dequant_block128_bf16", "quantize_export", "fp32_block128", "fp32_mxfp8_col", "moe_export",
                  "moe_grouped_export")
 
@@ -819,10 +823,11 @@ def run_profile(name: str, reps: int = 3):
             del x
             call = lib.plan_dequantize(d, torch.empty((ROWS, COLS), dtype=torch.bfloat16, device=dev),
                                        tile_scale_inv=s)
-        elif name == "mxfp8_col_dequant_bf16":
+        elif name in ("mxfp8_col_dequant_bf16", "mxfp8_col_dequant_fp32"):
             d, s = lib.mxfp8_col_direct(x, "swizzled")
             del x
-            call = lib.plan_dequantize(d, torch.empty((ROWS, COLS), dtype=torch.bfloat16, device=dev), scales=s,
+            odt = torch.bfloat16 if name == "mxfp8_col_dequant_bf16" else torch.float32
+            call = lib.plan_dequantize(d, torch.empty((ROWS, COLS), dtype=odt, device=dev), scales=s,
                                        layout="swizzled", columnwise=True)
         elif name == "mxfp4_dequant_bf16":
             p, s = lib.mxfp4_pack(x, "swizzled")

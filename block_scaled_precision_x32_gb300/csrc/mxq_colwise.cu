@@ -13,14 +13,21 @@
 // each row's two 1x32 blocks are read with full lines (a lane-per-row layout
 // touches 32 half lines per load, which the L1 pays for).  A block's two
 // lanes join their amax with one shuffle; each lane projects its chunks in
-// registers (the projection never goes back to HBM) and stages them in a
-// padded shared tile; lane t then scans the column pair (2t, 2t+1) over the
-// 32 rows with the packed NaN-propagating abs-max, and the lanes encode their
-// chunks with the bf16 multipliers 2^-s of the columns -- an exact product,
-// as the projected value has two significant bits -- and the E4M3 conversion.
-// Registers are capped at 64 so that 32 warps stay resident per SM.
-// fp32 input is loaded one row chunk at a time and projected through the
-// E2M1 conversion into the same bf16 values (f32_chunk_project).  Other
+// registers (the projection never goes back to HBM).  bf16 input: the lane
+// keeps its four projected chunks in registers and stages only their
+// column maxima over its four rows (packed NaN-propagating abs-max), so lane
+// t finds the 32x1 maxima of the column pair (2t, 2t+1) from 8 staged rows
+// (72 registers, at least 12 CTAs of 2 warps per SM; 32.8 against 34.3 us on
+// 8192 x 8192 with the whole projected tile staged, scanned over 32 rows
+// and read back).  fp32 input is loaded one row chunk at a time, projected
+// through the E2M1 conversion into the same bf16 values (f32_chunk_project)
+// and staged whole in a padded shared tile, which lane t scans over the 32
+// rows and the encode reads back (64 registers, held by its loads in
+// flight; staging four-row maxima besides the tile took 65.7 against
+// 51.9 us on 8192 x 8192).  The lanes
+// encode their chunks with the bf16 multipliers 2^-s of the columns -- an
+// exact product, as the projected value has two significant bits -- and
+// the E4M3 conversion.  Other
 // views (unaligned, or K % 32 != 0) use colwise_kernel: a warp per 32-row
 // band x 32 columns, a lane per row, the same steps.
 #include <cuda_runtime.h>
@@ -283,6 +290,11 @@ __device__ __forceinline__ uint32_t pack_halves(uint16_t lo, uint16_t hi) {
     return d;
 }
 
+// 8-byte global load that skips L1 allocation.
+__device__ __forceinline__ void ld8(uint32_t& lo, uint32_t& hi, const void* p) {
+    asm volatile("ld.global.L1::no_allocate.v2.b32 {%0,%1}, [%2];" : "=r"(lo), "=r"(hi) : "l"(p));
+}
+
 // bf16 2^-s (s in [-127, 127]: a normal, or the subnormal 2^-127); NaN for
 // a poisoned column block, so that its payloads convert to 0x7F.
 __device__ __forceinline__ uint32_t bf16_col_multiplier(uint32_t cm, int sx) {
@@ -317,16 +329,33 @@ __device__ __forceinline__ void f32_chunk_project(const uint32_t (&x)[16], int e
 constexpr int kTileWarps = 2;
 
 template <Elt ELT>
-__global__ void __launch_bounds__(32 * kTileWarps, 16) tile64_kernel(ColwiseArgs a, int64_t bands) {
+__global__ void __launch_bounds__(32 * kTileWarps, ELT == Elt::BF16 ? 12 : 16) tile64_kernel(ColwiseArgs a, int64_t bands) {
     constexpr int ES = ELT == Elt::BF16 ? 2 : 4;
     constexpr int RW = 32 + 4;  // words per staged row: 64 bf16 + 16 B pad (conflict-free 16-byte stores)
-    __shared__ __align__(16) uint32_t tile[kTileWarps][32 * RW];
+    constexpr bool F32 = ELT == Elt::FP32;
+    // fp32: the projected tile, scanned for the column maxima and read back by the
+    // encode; bf16 keeps its chunks in registers and stages only their column
+    // maxima over each lane's four rows
+    __shared__ __align__(16) uint32_t tile[kTileWarps][F32 ? 32 * RW : 8 * RW];
     __shared__ __align__(16) uint32_t colmul[kTileWarps][32];
     const int w = threadIdx.x >> 5, t = threadIdx.x & 31, q = t & 3, g = t >> 2;
     const int64_t nbr = (a.rows + 31) >> 5, Cpt = (nbr + 3) & ~int64_t(3);
     const int64_t col0 = ((int64_t)blockIdx.x * kTileWarps + w) * 64;  // first column of the warp tile
     const bool cvalid = col0 + 16 * q < a.K;                             // this lane's chunk is in the tensor
     const int64_t c0 = col0 + 2 * t;                                     // the column pair this lane scans
+    // scale offsets of columns c0 and c0 + 1 without their band term (c0 is even, so
+    // in the swizzled layout c0 + 1 sits 16 bytes further)
+    int64_t coff, cstep;
+    if (a.lay == 0) {
+        coff = c0 * nbr;
+        cstep = nbr;
+    } else if (a.lay == 1) {
+        coff = c0 * Cpt;
+        cstep = Cpt;
+    } else {
+        coff = (c0 >> 7) * (Cpt >> 2) * 512 + (c0 & 31) * 16 + ((c0 >> 5) & 3) * 4;
+        cstep = 16;
+    }
     uint32_t* trow = tile[w] + g * RW + 8 * q;
     if (a.skip != nullptr && *a.skip != 0) return;  // skip-update request: write nothing
 
@@ -334,6 +363,7 @@ __global__ void __launch_bounds__(32 * kTileWarps, 16) tile64_kernel(ColwiseArgs
         const int64_t rbase = band * 32 + g;  // rows rbase + 8i, i = 0..3
         const char* xp = static_cast<const char*>(a.x) + (rbase * a.ldx + col0 + 16 * q) * ES;
         const int64_t xstep = 8 * ES * a.ldx;  // 8 rows, in bytes
+        uint32_t y[4][8];  // bf16: the projected chunks, held until the encode
         if constexpr (ELT == Elt::FP32) {
             // one row chunk (16 fp32, two 32-byte loads) at a time, the next one in flight
             uint32_t x[16], nx[16];
@@ -356,14 +386,13 @@ __global__ void __launch_bounds__(32 * kTileWarps, 16) tile64_kernel(ColwiseArgs
                 for (int k = 0; k < 16; ++k) m = f32_absmax(m, x[k]);
                 m &= 0x7FFFFFFFu;
                 m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));  // the block's other half
-                uint32_t y[8];
-                f32_chunk_project(x, block_exponent<23>(m), m >= 0x7F800000u, y);
+                uint32_t yc[8];
+                f32_chunk_project(x, block_exponent<23>(m), m >= 0x7F800000u, yc);
                 uint32_t* d = trow + 8 * i * RW;
-                *reinterpret_cast<uint4*>(d) = make_uint4(y[0], y[1], y[2], y[3]);
-                *reinterpret_cast<uint4*>(d + 4) = make_uint4(y[4], y[5], y[6], y[7]);
+                *reinterpret_cast<uint4*>(d) = make_uint4(yc[0], yc[1], yc[2], yc[3]);
+                *reinterpret_cast<uint4*>(d + 4) = make_uint4(yc[4], yc[5], yc[6], yc[7]);
             }
         } else {
-            uint32_t y[4][8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 if (cvalid && rbase + 8 * i < a.rows) {
@@ -396,25 +425,29 @@ __global__ void __launch_bounds__(32 * kTileWarps, 16) tile64_kernel(ColwiseArgs
                         y[i][k] = pois ? 0x7FC07FC0u : bf2_mul(u, scl);
                     }
                 }
-                uint32_t* d = trow + 8 * i * RW;
-                *reinterpret_cast<uint4*>(d) = make_uint4(y[i][0], y[i][1], y[i][2], y[i][3]);
-                *reinterpret_cast<uint4*>(d + 4) = make_uint4(y[i][4], y[i][5], y[i][6], y[i][7]);
             }
+            // the lane's 16 columns, maximum over its four rows (sign bits arbitrary)
+            uint32_t pm[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) pm[k] = bf2_absmax(bf2_absmax(y[0][k], y[1][k]), bf2_absmax(y[2][k], y[3][k]));
+            *reinterpret_cast<uint4*>(trow) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
+            *reinterpret_cast<uint4*>(trow + 4) = make_uint4(pm[4], pm[5], pm[6], pm[7]);
         }
         __syncwarp();
 
-        // 32x1 maxima of the column pair (2t, 2t+1) and their scales
+        // 32x1 maxima of the column pair (2t, 2t+1) -- over the 32 staged rows (fp32) or
+        // the eight staged four-row maxima (bf16) -- and their scales
         uint32_t m2 = 0u;
 #pragma unroll
-        for (int rr = 0; rr < 32; ++rr) m2 = bf2_absmax(m2, tile[w][rr * RW + t]);
+        for (int rr = 0; rr < (F32 ? 32 : 8); ++rr) m2 = bf2_absmax(m2, tile[w][rr * RW + t]);
         m2 &= 0x7FFF7FFFu;
         const uint32_t cm0 = m2 & 0xFFFFu, cm1 = m2 >> 16;
         const int sx0 = host_exponent<7>(cm0), sx1 = host_exponent<7>(cm1);
         colmul[w][t] = bf16_col_multiplier(cm0, sx0) | (bf16_col_multiplier(cm1, sx1) << 16);
-        if (band < nbr) {
-            if (c0 < a.K) a.scales[scale_offset(c0, band, nbr, Cpt, a.lay)] = (uint8_t)(cm0 >= 0x7F80u ? 255 : sx0 + 127);
-            if (c0 + 1 < a.K)
-                a.scales[scale_offset(c0 + 1, band, nbr, Cpt, a.lay)] = (uint8_t)(cm1 >= 0x7F80u ? 255 : sx1 + 127);
+        if (band < nbr && c0 < a.K) {  // K is even: c0 + 1 is in the tensor too
+            uint8_t* sp = a.scales + coff + (a.lay == 2 ? ((band >> 2) << 9) + (band & 3) : band);
+            sp[0] = (uint8_t)(cm0 >= 0x7F80u ? 255 : sx0 + 127);
+            sp[cstep] = (uint8_t)(cm1 >= 0x7F80u ? 255 : sx1 + 127);
         }
         __syncwarp();
 
@@ -425,9 +458,16 @@ __global__ void __launch_bounds__(32 * kTileWarps, 16) tile64_kernel(ColwiseArgs
         uint8_t* dp = a.data + rbase * a.K + col0 + 16 * q;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t* d = trow + 8 * i * RW;
-            const uint4 ya = *reinterpret_cast<const uint4*>(d), yb = *reinterpret_cast<const uint4*>(d + 4);
-            const uint32_t yy[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
+            uint32_t yy[8];
+            if constexpr (F32) {
+                const uint32_t* d = trow + 8 * i * RW;
+                const uint4 ya = *reinterpret_cast<const uint4*>(d), yb = *reinterpret_cast<const uint4*>(d + 4);
+                yy[0] = ya.x, yy[1] = ya.y, yy[2] = ya.z, yy[3] = ya.w;
+                yy[4] = yb.x, yy[5] = yb.y, yy[6] = yb.z, yy[7] = yb.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) yy[k] = y[i][k];
+            }
             uint32_t b[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -482,129 +522,205 @@ __global__ void __launch_bounds__(kThreads) colwise_dequant_kernel(DequantArgs a
 }
 
 // Dequantize of the columnwise form, K % 32 == 0 and 32-byte aligned rows:
-// a CTA of 128 threads owns a 32-row band x 128 columns, a thread one row's
-// 32 columns (one 32-byte payload load; four threads cover a row's 128
-// bytes, so a warp load reads whole lines).  The band's 128 column scale
-// codes are loaded once per CTA and turned into bf16 multipliers
-// 2^(code-127) in shared memory; each element is then placed into a bf16
+// a CTA of 128 threads owns a 32-row band x 128 columns, four threads to a
+// row.  The band's 128 column codes become bf16 multipliers 2^(code-127) in
+// shared memory, built by every warp for itself when the scales are
+// swizzled (the 128 codes share four lines, so the extra loads hit L1 and no
+// CTA barrier is needed) and by warp 0 for the CTA otherwise (compact and
+// padded codes lie in 128 lines).  Each element is placed into a bf16
 // pattern as payload * 2^-120 (2^-112), multiplied exactly by 2^120 (2^112)
 // and once by its column's multiplier -- one rounding of the exact product,
-// as for the rowwise form.  A row chunk with a NaN / Inf payload or a
-// code-255 column, or (fp32 output) a column code below which products
-// leave bf16's normal range, takes the element-wise fp32 path.
-// Registers capped near 40 (12 CTAs per SM) and two bands per CTA: 33.8 us
-// on 8192 x 8192 bf16 out against 35.6 us at one band and 10 CTAs per SM
-// (38.3 us at the compiler's 72 registers; 14 or more CTAs per SM spill,
-// 48-62 us).  fp32 output, whose staging needs more registers, keeps 10 CTAs
-// per SM.
+// as for the rowwise form.  Whether a column code is 255 (or, for fp32
+// output, below the code under which products leave bf16's normal range) is
+// one warp vote over the lanes that loaded the codes.  Such a chunk, or one
+// with a NaN / Inf payload, takes the element-wise fp32 path.
+// bf16 output: a thread takes one row's 32 columns of chunk q (one 32-byte
+// payload load; four threads cover a row's 128 bytes, so a warp load reads
+// whole lines).  fp32 output: thread q of a row takes columns 8q..8q+7 of
+// each 32-column group, so that the four threads of a row store 128
+// contiguous bytes per instruction (128 bytes per thread stored as four
+// 32-byte pieces of one chunk touched 32 lines per warp store: 66.7 against
+// 51.1 us on 8192 x 8192).  One band per CTA; 12 (bf16) / 10 (fp32) CTAs
+// per SM.  8192 x 8192 to bf16: 31.0 us, against 33.9 us with the codes
+// loaded once per CTA behind a barrier and tested code by code per thread.
 constexpr int kDqThreads = 128;
-constexpr int kDqBandsPerCta = 2;
 
-template <bool E5M2, bool BF16OUT>
+template <bool E5M2, bool BF16OUT, bool PERWARP>
 __global__ void __launch_bounds__(kDqThreads, BF16OUT ? 12 : 10) colwise_dequant_tile_kernel(DequantArgs a, int64_t bands) {
-    // multiplier words of chunk q at 16 q + 4 (q / 2): the four chunks' words
-    // read by one warp instruction fall in different banks
-    __shared__ __align__(16) uint32_t colmul[64 + 8];
-    __shared__ __align__(16) uint32_t colcode[32];  // codes, four columns per word
-    const int t = threadIdx.x, q = t & 3, rr = t >> 2;
+    // the multiplier words of chunk q at 16 q + 4 (q / 2) -- the four chunks'
+    // words read by one warp instruction fall in different banks -- and the
+    // codes, four columns per word: one copy per warp (PERWARP) or per CTA
+    constexpr int kW = PERWARP ? kDqThreads / 32 : 1;
+    __shared__ __align__(16) uint32_t colmul[kW][64 + 8];
+    __shared__ __align__(16) uint32_t colcode[kW][32];
+    __shared__ uint32_t slow_sh;
+    const int t = threadIdx.x & 31, w = threadIdx.x >> 5, q = t & 3, rr = threadIdx.x >> 2;
+    const int ww = PERWARP ? w : 0;
     const int64_t nbr = (a.rows + 31) >> 5, Cpt = (nbr + 3) & ~int64_t(3);
     const int64_t col0 = (int64_t)blockIdx.x * 128;
     const bool cvalid = col0 + 32 * q < a.K;
     constexpr uint32_t kMinCode = E5M2 ? 17u : 10u;  // fp32 output: smallest code kept on the bf16 path
     constexpr uint32_t fix = E5M2 ? 0x77807780u : 0x7B807B80u;  // 2^112 / 2^120, both halves
+    // lane t loads the codes of columns cA .. cA + 3; their scale offsets without the band
+    // term are coff + u * cstep (cA is a multiple of 4: in the swizzled layout the four
+    // sit 16 bytes apart)
+    const int64_t cA = col0 + 4 * t;
+    int64_t coff, cstep;
+    if (a.lay == 0) {
+        coff = cA * nbr;
+        cstep = nbr;
+    } else if (a.lay == 1) {
+        coff = cA * Cpt;
+        cstep = Cpt;
+    } else {
+        coff = (cA >> 7) * (Cpt >> 2) * 512 + (cA & 31) * 16 + ((cA >> 5) & 3) * 4;
+        cstep = 16;
+    }
+    const int mbase = 16 * (t >> 3) + 4 * (t >> 4) + 2 * (t & 7);  // multiplier words of columns cA..cA+3
     for (int64_t band = blockIdx.y; band < bands; band += gridDim.y) {
         const int64_t r = band * 32 + rr;
         const bool rvalid = cvalid && r < a.rows;
+        // bf16 output: the row's 32 payload bytes of chunk q; fp32 output: bytes 8q..8q+7 of
+        // each 32-column group gg in words 2gg, 2gg+1 (the four lanes of a row then store
+        // 128 contiguous bytes per instruction).  In flight while the scales are prepared.
         uint32_t pw[8];
-        if (rvalid) ld32(pw, a.data + r * a.K + col0 + 32 * q);  // in flight while the scales are prepared
-        if (t < 32) {
-            uint32_t codes = 0u;
+        if constexpr (BF16OUT) {
+            if (rvalid) ld32(pw, a.data + r * a.K + col0 + 32 * q);
+        } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t c = col0 + 4 * t + u;
-                const uint32_t code = c < a.K ? a.scales[scale_offset(c, band, nbr, Cpt, a.lay)] : 0u;
-                codes |= code << (8 * u);
+            for (int gg = 0; gg < 4; ++gg) {
+                pw[2 * gg] = pw[2 * gg + 1] = 0u;
+                if (r < a.rows && col0 + 32 * gg < a.K) ld8(pw[2 * gg], pw[2 * gg + 1], a.data + r * a.K + col0 + 32 * gg + 8 * q);
             }
-            colcode[t] = codes;
-            const int base = 16 * (t >> 3) + 4 * (t >> 4) + 2 * (t & 7);  // words of columns 4t..4t+3
-            colmul[base] = (bf16_scale_pair(codes & 0xFFu) & 0xFFFFu) | (bf16_scale_pair((codes >> 8) & 0xFFu) << 16);
-            colmul[base + 1] =
-                (bf16_scale_pair((codes >> 16) & 0xFFu) & 0xFFFFu) | (bf16_scale_pair(codes >> 24) << 16);
         }
-        __syncthreads();
-        if (rvalid) {
-            bool slow = false;
+        uint32_t slowmask = 0u;  // bit 8q + j: lane 8q + j, which holds codes of chunk q, found a slow code
+        if (PERWARP || w == 0) {
+            uint32_t codes = 0u;
+            if (cA < a.K) {  // K % 32 == 0: all four columns are in the tensor
+                const uint8_t* sp = a.scales + coff + (a.lay == 2 ? ((band >> 2) << 9) + (band & 3) : band);
+                codes = (uint32_t)sp[0] | ((uint32_t)sp[cstep] << 8) | ((uint32_t)sp[2 * cstep] << 16) |
+                        ((uint32_t)sp[3 * cstep] << 24);
+            }
+            // a code 255 (a zero byte of ~codes) or, for fp32 output, a code below kMinCode:
+            // the byte tests are exact for "some byte", which is all that is asked
+            uint32_t bad = (~codes - 0x01010101u) & codes & 0x80808080u;
+            if constexpr (!BF16OUT) bad |= (codes - 0x01010101u * kMinCode) & ~codes & 0x80808080u;
+            slowmask = __ballot_sync(0xffffffffu, bad != 0u);
+            colcode[ww][t] = codes;
+            colmul[ww][mbase] = (bf16_scale_pair(codes & 0xFFu) & 0xFFFFu) | (bf16_scale_pair((codes >> 8) & 0xFFu) << 16);
+            colmul[ww][mbase + 1] =
+                (bf16_scale_pair((codes >> 16) & 0xFFu) & 0xFFFFu) | (bf16_scale_pair(codes >> 24) << 16);
+            if (!PERWARP && t == 0) slow_sh = slowmask;
+        }
+        if constexpr (PERWARP) {
+            __syncwarp();
+        } else {
+            __syncthreads();
+            slowmask = slow_sh;
+        }
+        if constexpr (BF16OUT) {
+            if (rvalid) {
+                const bool slow = ((slowmask >> (8 * q)) & 0xFFu) != 0u;
+                uint32_t sp = 0u;
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const uint32_t cw = colcode[8 * q + m];
+                for (int k = 0; k < 8; ++k) sp |= special_bytes<E5M2>(pw[k]);
+                char* op = static_cast<char*>(a.out) + (r * a.K + col0 + 32 * q) * 2;
+                if (sp == 0u && !slow) {
+                    const uint32_t* mw = colmul[ww] + 16 * q + 4 * (q >> 1);
+                    uint32_t mreg[16];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t code = (cw >> (8 * u)) & 0xFFu;
-                    slow |= code == 255u;
-                    if constexpr (!BF16OUT) slow |= code < kMinCode;
+                    for (int m = 0; m < 4; ++m) {
+                        const uint4 mm = *reinterpret_cast<const uint4*>(mw + 4 * m);
+                        mreg[4 * m] = mm.x;
+                        mreg[4 * m + 1] = mm.y;
+                        mreg[4 * m + 2] = mm.z;
+                        mreg[4 * m + 3] = mm.w;
+                    }
+#pragma unroll
+                    for (int s8 = 0; s8 < 2; ++s8) {
+                        uint32_t seg[8];
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const int pidx = 8 * s8 + v;  // column pair within the chunk
+                            const uint32_t pr = place_pair<E5M2>(pw[pidx >> 1], (pidx & 1) ? 0x4342u : 0x4140u);
+                            seg[v] = bf2_mul(bf2_mul(pr, fix), mreg[pidx]);
+                        }
+                        st32(op + 32 * s8, seg);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int s8 = 0; s8 < 2; ++s8) {
+                        uint32_t seg[8];
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            uint32_t o = 0u;
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const int e = 16 * s8 + 2 * v + hh;  // element of the chunk
+                                const uint32_t code = (colcode[ww][8 * q + (e >> 2)] >> (8 * (e & 3))) & 0xFFu;
+                                const uint32_t scale = code == 255u ? 0x7FC00000u : f32_pow2((int)code - 127);
+                                const uint32_t f = decode_scaled<E5M2>((pw[e >> 2] >> (8 * (e & 3))) & 0xFFu, scale);
+                                o |= bf16_rne(f) << (16 * hh);
+                            }
+                            seg[v] = o;
+                        }
+                        st32(op + 32 * s8, seg);
+                    }
                 }
             }
+        } else if (r < a.rows) {
+            // any slow code among the band's columns, or a NaN / Inf payload: element-wise
             uint32_t sp = 0u;
 #pragma unroll
             for (int k = 0; k < 8; ++k) sp |= special_bytes<E5M2>(pw[k]);
-            char* op = static_cast<char*>(a.out) + (r * a.K + col0 + 32 * q) * (BF16OUT ? 2 : 4);
-            if (sp == 0u && !slow) {
-                const uint32_t* mw = colmul + 16 * q + 4 * (q >> 1);
-                uint32_t mreg[16];
+            const bool slow = slowmask != 0u || sp != 0u;
+            char* op = static_cast<char*>(a.out) + (r * a.K + col0 + 8 * q) * 4;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const uint4 mm = *reinterpret_cast<const uint4*>(mw + 4 * m);
-                    mreg[4 * m] = mm.x;
-                    mreg[4 * m + 1] = mm.y;
-                    mreg[4 * m + 2] = mm.z;
-                    mreg[4 * m + 3] = mm.w;
-                }
+            for (int gg = 0; gg < 4; ++gg) {
+                if (col0 + 32 * gg >= a.K) break;
+                uint32_t seg[8];
+                if (!slow) {
+                    // columns 32gg + 8q .. + 7: multiplier words 4q .. 4q + 3 of chunk gg
+                    const uint4 mm = *reinterpret_cast<const uint4*>(colmul[ww] + 16 * gg + 4 * (gg >> 1) + 4 * q);
+                    const uint32_t mreg[4] = {mm.x, mm.y, mm.z, mm.w};
 #pragma unroll
-                for (int s8 = 0; s8 < (BF16OUT ? 2 : 4); ++s8) {
-                    uint32_t seg[8];
-#pragma unroll
-                    for (int v = 0; v < (BF16OUT ? 8 : 4); ++v) {
-                        const int pidx = (BF16OUT ? 8 : 4) * s8 + v;  // column pair within the chunk
-                        const uint32_t pr = place_pair<E5M2>(pw[pidx >> 1], (pidx & 1) ? 0x4342u : 0x4140u);
-                        const uint32_t y = bf2_mul(bf2_mul(pr, fix), mreg[pidx]);
-                        if constexpr (BF16OUT) {
-                            seg[v] = y;
-                        } else {
-                            seg[2 * v] = y << 16;
-                            seg[2 * v + 1] = y & 0xFFFF0000u;
-                        }
+                    for (int v = 0; v < 4; ++v) {
+                        const uint32_t pr = place_pair<E5M2>(pw[2 * gg + (v >> 1)], (v & 1) ? 0x4342u : 0x4140u);
+                        const uint32_t y = bf2_mul(bf2_mul(pr, fix), mreg[v]);
+                        seg[2 * v] = y << 16;
+                        seg[2 * v + 1] = y & 0xFFFF0000u;
                     }
-                    st32(op + 32 * s8, seg);
-                }
-            } else {
-#pragma unroll 1
-                for (int s8 = 0; s8 < (BF16OUT ? 2 : 4); ++s8) {
-                    uint32_t seg[8];
+                } else {
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        uint32_t o = 0u;
-#pragma unroll
-                        for (int hh = 0; hh < (BF16OUT ? 2 : 1); ++hh) {
-                            const int e = BF16OUT ? 16 * s8 + 2 * v + hh : 8 * s8 + v;  // element of the chunk
-                            const uint32_t code = (colcode[8 * q + (e >> 2)] >> (8 * (e & 3))) & 0xFFu;
-                            const uint32_t scale = code == 255u ? 0x7FC00000u : f32_pow2((int)code - 127);
-                            const uint32_t f = decode_scaled<E5M2>((pw[e >> 2] >> (8 * (e & 3))) & 0xFFu, scale);
-                            if constexpr (BF16OUT)
-                                o |= bf16_rne(f) << (16 * hh);
-                            else
-                                o = f;
-                        }
-                        seg[v] = o;
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t code = (colcode[ww][8 * gg + 2 * q + (j >> 2)] >> (8 * (j & 3))) & 0xFFu;
+                        const uint32_t scale = code == 255u ? 0x7FC00000u : f32_pow2((int)code - 127);
+                        seg[j] = decode_scaled<E5M2>((pw[2 * gg + (j >> 2)] >> (8 * (j & 3))) & 0xFFu, scale);
                     }
-                    st32(op + 32 * s8, seg);
                 }
+                st32(op + 128 * gg, seg);
             }
         }
-        __syncthreads();  // colmul / colcode are rewritten by the next band
+        // colmul / colcode / slow_sh are rewritten by the next band
+        if constexpr (PERWARP)
+            __syncwarp();
+        else
+            __syncthreads();
     }
 }
 
 bool aligned(const void* p, int64_t n) { return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)n) == 0; }
+
+template <bool PERWARP>
+cudaError_t launch_dequant_tile(const DequantArgs& a, bool e5, dim3 grid, int64_t bands, cudaStream_t s) {
+    if (e5)
+        a.out_bf16 ? colwise_dequant_tile_kernel<true, true, PERWARP><<<grid, kDqThreads, 0, s>>>(a, bands)
+                   : colwise_dequant_tile_kernel<true, false, PERWARP><<<grid, kDqThreads, 0, s>>>(a, bands);
+    else
+        a.out_bf16 ? colwise_dequant_tile_kernel<false, true, PERWARP><<<grid, kDqThreads, 0, s>>>(a, bands)
+                   : colwise_dequant_tile_kernel<false, false, PERWARP><<<grid, kDqThreads, 0, s>>>(a, bands);
+    return cudaGetLastError();
+}
 
 template <Elt ELT, bool VEC, int DST>
 cudaError_t launch_one(const ColwiseArgs& a, cudaStream_t s) {
@@ -642,16 +758,13 @@ cudaError_t launch_colwise_dequant(const DequantArgs& a, cudaStream_t s) {
     const bool e5 = a.fp8 == 1;
     const int oes = a.out_bf16 ? 2 : 4;
     if (a.K % 32 == 0 && aligned(a.data, 32) && aligned(a.out, 32) && (a.K * oes) % 32 == 0) {
+        // swizzled scales: every warp loads the band's codes itself (they share 4 lines);
+        // compact / padded ones lie in 128 different lines, loaded once per CTA
         const int64_t bands = ceil_div(a.rows, 32), gx = ceil_div(a.K, 128);
-        const int64_t gy = ceil_div(bands, kDqBandsPerCta);
-        const dim3 grid((unsigned)gx, (unsigned)(gy < 65535 ? gy : 65535));
-        if (e5)
-            a.out_bf16 ? colwise_dequant_tile_kernel<true, true><<<grid, kDqThreads, 0, s>>>(a, bands)
-                       : colwise_dequant_tile_kernel<true, false><<<grid, kDqThreads, 0, s>>>(a, bands);
-        else
-            a.out_bf16 ? colwise_dequant_tile_kernel<false, true><<<grid, kDqThreads, 0, s>>>(a, bands)
-                       : colwise_dequant_tile_kernel<false, false><<<grid, kDqThreads, 0, s>>>(a, bands);
-        return cudaGetLastError();
+        const dim3 grid((unsigned)gx, (unsigned)(bands < 65535 ? bands : 65535));
+        if (a.lay == 2)
+            return launch_dequant_tile<true>(a, e5, grid, bands, s);
+        return launch_dequant_tile<false>(a, e5, grid, bands, s);
     }
     const int64_t total = ceil_div(a.rows, 32) * a.K;
     int64_t grid = ceil_div(total, (int64_t)kThreads);

@@ -333,6 +333,40 @@ def test_dequant_columnwise_every_payload_and_scale_code(mx, K, lay, kind):
         np.testing.assert_array_equal(host_bits(got), oracle_bits(np.ascontiguousarray(want)))
 
 
+@pytest.mark.parametrize("K", [224, 288, 416])
+@pytest.mark.parametrize("lay", LAYOUTS)
+@pytest.mark.parametrize("kind", [oracle.E4M3, oracle.E5M2])
+def test_dequant_columnwise_fast_and_slow_chunks(mx, K, lay, kind):
+    """Columnwise dequantize on widths that end in a partial 128-column
+    tile (K % 32 == 0, K % 128 != 0), 200 rows (a ragged last band).  Most
+    bands hold only codes of the fast path; band 2 has one code 255 in one
+    column, band 4 one code below the fp32 fast range, band 6 (the ragged
+    one) a code 0; rows 37 and 150 hold NaN / Inf payloads.  bf16 and fp32
+    output, every layout (swizzled codes are loaded per warp, compact and
+    padded ones per CTA)."""
+    rows = 200
+    g = np.random.default_rng(K * 7 + kind * 5 + lay)
+    special = (lambda b: (b & 0x7F) == 0x7F) if kind == oracle.E4M3 else (lambda b: (b & 0x7C) == 0x7C)
+    data = g.integers(0, 256, size=(rows, K), dtype=np.uint8)
+    data[special(data)] &= 0x83  # finite payloads everywhere ...
+    for r in (37, 150):  # ... but in two rows
+        cols = g.choice(K, size=3, replace=False)
+        data[r, cols] = 0x7F if kind == oracle.E4M3 else np.array([0x7C, 0xFC, 0x7E], dtype=np.uint8)
+    nbr = (rows + 31) // 32
+    cs = g.integers(20, 231, size=(K, nbr), dtype=np.uint8)  # K x nbr codes
+    cs[5, 2] = 255
+    cs[K - 3, 4] = 3
+    cs[100, 6] = 0
+    scales = cs.reshape(-1) if lay == oracle.COMPACT else oracle.scales_to_layout(cs, K, rows, lay)
+    d = torch.from_numpy(data).cuda()
+    s = torch.from_numpy(scales).cuda()
+    for odt, ocode in ((torch.float32, oracle.FP32), (torch.bfloat16, oracle.BF16)):
+        got = mx.dequantize(d, scales=s, layout=lay, fp8="e4m3" if kind == oracle.E4M3 else "e5m2", out_dtype=odt,
+                            columnwise=True)
+        want = oracle.dequant_mxfp8(np.ascontiguousarray(data.T), cs, oracle.COMPACT, kind, ocode).T
+        np.testing.assert_array_equal(host_bits(got), oracle_bits(np.ascontiguousarray(want)))
+
+
 def test_dequant_block128_arbitrary_scales(mx):
     """Blockwise dequantize with scale_inv that are not powers of two
     (rounded fp32 products, subnormal results, overflow to Inf)."""
