@@ -8,7 +8,10 @@
 // Swizzled input, nb >= 16, scales and output 16-byte aligned (the usual
 // case: every GEMM-swizzled weight with K >= 512): the chunk kernel below,
 // which needs no shared memory -- each lane turns 16-byte loads of four rows'
-// scales into aligned 16-byte chunks of those rows' compact output.
+// scales into aligned 16-byte chunks of those rows' compact output -- or,
+// for large exports (bulk_wins), the bulk kernel, which stages whole row
+// tiles in shared memory by bulk copies so that global memory sees only
+// whole-tile reads and contiguous writes.
 // Other swizzled input: one CTA per (128-row tile, group of 16 column
 // tiles).  The group's bytes are contiguous in the swizzled buffer (16 x 512),
 // so they are staged in shared memory with 16-byte loads -- each 512-byte tile
@@ -20,9 +23,9 @@
 // range -- as aligned words.
 // Padded input: one warp per row, lanes on consecutive bytes.
 // Grouped export: up to kGroupedMax storages per launch, their descriptors
-// passed by value in the kernel parameters; chunk-path storages run the chunk
-// kernel's code, the others a byte copy; every storage's row tiles are walked
-// with a grid stride.
+// passed by value in the kernel parameters; chunk-path storages run the bulk
+// or the chunk kernel's code, the others a byte copy; every storage's row
+// tiles are walked with a grid stride.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -317,6 +320,231 @@ __global__ void __launch_bounds__(kChunkThreads) unswizzle_chunk_kernel(ExportAr
         unswizzle_chunks<CPW>(a, rt, cg, a.scales + rt * ct * 512);
 }
 
+// Swizzled input with many row tiles (nb >= 16, 16-byte aligned scales and
+// output): the bulk kernel.  A CTA stages one 128-row tile: one thread copies
+// the tile's ct * 512 swizzled bytes -- contiguous -- into shared memory with
+// one bulk copy (cp.async.bulk, completed on an mbarrier); the CTA turns them
+// into the tile's compact rows with the chunk kernel's arithmetic (16-byte
+// shared loads of four rows' words, funnel shifts, 16-byte shared stores) in
+// two parts of 64 rows, and one thread writes each part -- 64 nb contiguous
+// bytes of the output, 16-byte aligned -- with one bulk store.  Global memory
+// sees whole-tile reads and contiguous writes, in place of the chunk
+// kernel's 16-byte stores to 32 different rows per warp instruction.
+// With kBulkThreads a multiple of 32 a thread always holds the same lane q,
+// so everything that depends on q alone is computed once per kernel (3.4 M
+// warp instructions on the MoE stack against 4.7 M recomputing it per
+// chunk).  Measured on the 32 x 4096 x 7184 MoE stack with inputs larger
+// than L2: one CTA of 128 threads per row tile, five resident per SM, 12.8 us
+// against 13.4 us for the chunk kernel; the whole tile staged as one part
+// (three CTAs per SM) 15.7 us, four 32-row parts (six per SM) 15.1 us, and
+// persistent CTAs with two or three tiles' copies in flight 15.5-18.3 us.
+// The mbarrier wait is bounded (about a second of SM clocks): a tile whose
+// copy has not landed by then is written as 0xFF bytes (the E8M0 NaN code),
+// the copy is waited for once more, bounded again, and the CTA stops.
+constexpr int kBulkThreads = 128;
+static_assert(kBulkThreads % 32 == 0, "a thread keeps one lane q for every tile");
+
+// Shared memory of the bulk kernel: the mbarrier (padded to 128 bytes), the
+// swizzled tile -- ROT: and 2 KB past it, so that a row's last chunk reads
+// up to four column tiles beyond the tile without a test (those bytes are
+// shifted or merged away) -- and one 64-row part of compact output with 16
+// spare bytes (the part's last chunk may run up to 15 bytes past it).
+// Unrotated, the last chunk tests its column tiles instead: the 2 KB would
+// cost the MoE stack's nb = 225 its fifth CTA per SM (13.05 against 12.8 us);
+// rotated, lanes reach their last chunk in different steps and the test
+// diverges (13.4 against 12.7 us at nb = 256, four CTAs per SM either way).
+int64_t bulk_smem_bytes(int64_t nb, bool rot) {
+    return 128 + ((nb + 3) >> 2) * 512 + (rot ? 2048 : 0) + ((64 * nb + 15) & ~int64_t(15)) + 16;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Wait for phase `parity` of the mbarrier at `mbar` to complete; false after about 2^31 SM clocks.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t mbar, uint32_t parity) {
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t done;
+        asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                     : "=r"(done)
+                     : "r"(mbar), "r"(parity)
+                     : "memory");
+        if (done) return true;
+        if (clock64() - t0 > (1ll << 31)) return false;
+    }
+}
+
+// What a thread's lane q fixes: row q of each row group s (rows q + 32 s)
+// starts its compact output b bytes before a 16-byte boundary's chunk 0,
+// ends in chunk ilast with e bytes of it inside the row (e < 16: the chunk
+// closes the row with the next row's first 16 - e bytes), and its chunk i
+// reads column tiles 4 i + b / 4 .. 4 i + b / 4 + 4 of the tile.
+struct BulkLane {
+    int q, b, sh, ilast, e, rot;
+    int src;  // byte offset in the staged tile of chunk 0's first word: 512 (b / 4) + 16 q
+    int dst;  // byte offset in a staged part of row q's chunk 0: q nb + b
+};
+
+__device__ __forceinline__ BulkLane bulk_lane(int nb) {
+    BulkLane L;
+    const int n16 = nb & 15;
+    L.q = threadIdx.x & 31;
+    L.b = (16 - ((L.q * n16) & 15)) & 15;
+    L.sh = 8 * (L.b & 3);
+    L.ilast = (nb - 1 - L.b) >> 4;
+    L.e = 16 - ((16 - (((L.q + 1) * n16) & 15)) & 15);
+    L.rot = (L.q - ((L.q * nb + 15) >> 4)) & 7;
+    L.src = 512 * (L.b >> 2) + 16 * L.q;
+    L.dst = L.q * nb + L.b;
+    return L;
+}
+
+// Chunk i of row group S of the staged words w (lane q) -> the part staged at `ob`.
+template <int S>
+__device__ __forceinline__ void bulk_chunk(const uint4 (&w)[5], const uint4* h, int e, int sh, uint8_t* dst) {
+    uint32_t o[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) o[t] = __funnelshift_r(word_of(w[t], S), word_of(w[t + 1], S), sh);
+    if (h != nullptr) {
+        const uint32_t hw[4] = {word_of(h[0], S), word_of(h[1], S), word_of(h[2], S), word_of(h[3], S)};
+        merge_next_row(o, hw, e);
+    }
+    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Chunk indices 0..N-1 (ilast <= N - 1).  A 16-byte shared access is served
+// eight lanes at a time, conflict-free when the eight hit distinct 16-byte
+// units mod 8.  Lane q's loads sit at unit 32 jt + q (distinct for eight
+// consecutive q); its row's chunk i at unit ceil((q + 32 s) nb / 16) + i,
+// which for one i can collide across q: 2-way at most for most nb (225,
+// 240), 8-way for nb = 256.  ROT (chosen by the host where a store would
+// collide 4-way or worse): lane q takes chunk (i' + rot_q) mod N in step i',
+// rot_q = (q - ceil(q nb / 16)) mod 8, so that its unit is q + i' + 2 s nb
+// mod 8 -- distinct again, up to the wrap at N.  Rotated, the chunks that
+// close a row with the next row's first bytes would fall in different steps
+// for different lanes, and their merge is long, so they take a step of
+// their own after the others; unrotated, they are the last step's chunks.
+template <bool ROT>
+__device__ bool bulk_tile(const ExportArgs& a, int64_t rt, uint8_t* in, uint8_t* ob, uint32_t mb, uint32_t parity,
+                          const BulkLane& L, int* ok) {
+    const int nb = (int)((a.K + 31) >> 5), ct = (nb + 3) >> 2;
+    const int64_t r0 = rt * 128;
+    const int nrows = (int)min((int64_t)128, a.rows - r0);
+    if (threadIdx.x == 0) {
+        const int in_bytes = ct * 512;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(in_bytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(smem_addr(in)), "l"(a.scales + rt * in_bytes), "r"(in_bytes), "r"(mb)
+                     : "memory");
+        *ok = mbar_wait_bounded(mb, parity) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*ok) {
+        for (int64_t k = threadIdx.x; k < (int64_t)nrows * nb; k += kBulkThreads) a.out[r0 * nb + k] = 0xFF;
+        if (threadIdx.x == 0) mbar_wait_bounded(mb, parity);  // the copy in flight, if it still lands
+        return false;
+    }
+    // every thread observes the completed phase itself (acquire) before reading the tile
+    asm volatile("{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%0], %1; }" ::"r"(mb), "r"(parity)
+                 : "memory");
+    const int N = ((nb - 1) >> 4) + 1;
+    const int steps = N + (ROT && (nb & 15) != 0 ? 1 : 0);
+    const bool has_cross = L.e < 16;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+        const int pr0 = 64 * part;  // rows q + 32 s, s = 2 part, 2 part + 1
+        if (pr0 >= nrows) break;
+        if (pr0 + L.q < nrows) {
+            const bool second = pr0 + 32 + L.q < nrows;
+            for (int ip = threadIdx.x >> 5; ip < steps; ip += kBulkThreads / 32) {
+                int i;
+                bool cross;
+                if constexpr (ROT) {
+                    if (ip >= N) {
+                        if (!has_cross) continue;
+                        i = L.ilast;
+                        cross = true;
+                    } else {
+                        i = ip + L.rot;
+                        if (i >= N) i = i - N < N ? i - N : i % N;
+                        if (i > L.ilast - (has_cross ? 1 : 0)) continue;
+                        cross = false;
+                    }
+                } else {
+                    i = ip;
+                    if (i > L.ilast) continue;
+                    cross = has_cross && i == L.ilast;
+                }
+                const uint8_t* src = in + L.src + 2048 * i;
+                uint4 w[5];
+                if (ROT || i < L.ilast) {  // column tiles 4 i + b / 4 + 4 <= ct - 1, or within the 2 KB past them
+#pragma unroll
+                    for (int t = 0; t < 5; ++t) w[t] = *reinterpret_cast<const uint4*>(src + 512 * t);
+                } else {  // the row's last chunk: column tiles past the tile hold only bytes past the row
+                    const int jt0 = 4 * i + (L.b >> 2);
+#pragma unroll
+                    for (int t = 0; t < 5; ++t)
+                        w[t] = jt0 + t < ct ? *reinterpret_cast<const uint4*>(src + 512 * t) : make_uint4(0u, 0u, 0u, 0u);
+                }
+                uint4 h[4];
+                if (cross) {  // the next rows' first 16 bytes: column tiles 0..3 of lane q + 1 (q < 31)
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) h[t] = *reinterpret_cast<const uint4*>(in + 16 * (L.q + 1) + 512 * t);
+                }
+                uint8_t* dst = ob + L.dst + 16 * i;
+                if (part == 0) {
+                    bulk_chunk<0>(w, cross ? h : nullptr, L.e, L.sh, dst);
+                    if (second) bulk_chunk<1>(w, cross ? h : nullptr, L.e, L.sh, dst + 32 * nb);
+                } else {
+                    bulk_chunk<2>(w, cross ? h : nullptr, L.e, L.sh, dst);
+                    if (second) bulk_chunk<3>(w, cross ? h : nullptr, L.e, L.sh, dst + 32 * nb);
+                }
+            }
+        }
+        // the part's bytes (and, after the last part, the tile's reads) are done: hand them to the copy engine
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        const int tot = (min(nrows, pr0 + 64) - pr0) * nb, main16 = tot & ~15;
+        uint8_t* gout = a.out + (r0 + pr0) * nb;
+        if (threadIdx.x == 0 && main16 > 0) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gout), "r"(smem_addr(ob)),
+                         "r"(main16)
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        for (int k = main16 + threadIdx.x; k < tot; k += kBulkThreads) gout[k] = ob[k];  // the tensor's last bytes
+        if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncthreads();  // the output part is rewritten next
+    }
+    return true;
+}
+
+// A CTA's row tiles rt0, rt0 + stride, ... (one, when the grid has a CTA per
+// tile), each through the same buffers and alternating mbarrier phases.
+template <bool ROT>
+__device__ void bulk_walk(const ExportArgs& a, int64_t tiles_r, int64_t rt0, int64_t stride, uint8_t* sm, int* ok) {
+    const int nb = (int)((a.K + 31) >> 5);
+    uint8_t* in = sm + 128;
+    uint8_t* ob = in + ((nb + 3) >> 2) * 512 + (ROT ? 2048 : 0);
+    const uint32_t mb = smem_addr(sm);
+    const BulkLane L = bulk_lane(nb);
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mb) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    uint32_t parity = 0;
+    for (int64_t rt = rt0; rt < tiles_r; rt += stride, parity ^= 1u)
+        if (!bulk_tile<ROT>(a, rt, in, ob, mb, parity, L, ok)) return;
+    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+template <bool ROT>
+__global__ void __launch_bounds__(kBulkThreads) bulk_export_kernel(ExportArgs a, int64_t tiles_r) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    __shared__ int ok;
+    bulk_walk<ROT>(a, tiles_r, blockIdx.x, gridDim.x, sm, &ok);
+}
+
 // Largest staging area of the flat kernel (bytes of dynamic shared memory).
 constexpr int kFlatSmemMax = 160 * 1024;
 
@@ -337,15 +565,30 @@ __global__ void __launch_bounds__(kThreads) unpad_kernel(ExportArgs a) {
 
 // Many storages in one launch: blockIdx.z picks the storage, blockIdx.x
 // walks its 128-row tiles (grid stride, so any number of them), blockIdx.y
-// its chunk groups.  A storage the chunk path takes (the host sets path 1:
-// swizzled, nb >= 16, 16-byte aligned scales and output) runs it as the
-// single export does; any other swizzled or padded storage is copied byte by
-// byte by the blockIdx.y == 0 CTAs.
+// its chunk groups.  The host sets each storage's path: 2 and 3 (bulk,
+// unrotated and rotated: the launch's chunk-eligible storages hold many row
+// tiles in total) and 1
+// (chunk: swizzled, nb >= 16, 16-byte aligned scales and output) run the
+// single export's code -- the bulk path in the blockIdx.y == 0 CTAs, with
+// the launch's dynamic shared memory; any other swizzled or padded storage
+// is copied byte by byte by the blockIdx.y == 0 CTAs.
+static_assert(kChunkThreads == kBulkThreads, "the grouped kernel runs both paths with one block size");
+
 template <int CPW>
 __global__ void __launch_bounds__(kChunkThreads) grouped_export_kernel(GroupedExport b) {
+    extern __shared__ __align__(128) uint8_t sm[];  // bulk path only
+    __shared__ int ok;
     const ExportArgs& a = b.item[blockIdx.z];
     const int64_t nb = (a.K + 31) >> 5, Cp = (nb + 3) & ~int64_t(3);
     const int64_t tr = (a.rows + 127) >> 7;
+    if (a.path >= 2) {
+        if (blockIdx.y != 0) return;
+        if (a.path == 3)
+            bulk_walk<true>(a, tr, blockIdx.x, gridDim.x, sm, &ok);
+        else
+            bulk_walk<false>(a, tr, blockIdx.x, gridDim.x, sm, &ok);
+        return;
+    }
     if (a.path == 1) {
         const int64_t ngroups = ((nb + 15) / 16 + CPW - 1) / CPW;
         const int64_t cg = (int64_t)blockIdx.y * (kChunkThreads / 32) + (threadIdx.x >> 5);
@@ -391,11 +634,12 @@ cudaError_t launch_flat(const ExportArgs& a, int64_t tr, int64_t grid, int64_t s
 // scales and output.  Chunks per warp (CPW), measured on GB300: 2 for small
 // exports (up to 8 such warps per SM; 8192 x 8192: 2.3 us against 2.6 us at
 // 1), else 1 (the 32 x 4096 x 7184 MoE stack: 13.6 us against 14.4 us at 2
-// and 14.2 us at 4 or 8).  Also measured and dropped: 32-byte chunks (whole
-// sector stores; 150+ registers, 20.9 us against 16.9 us for that build's
-// 16-byte chunks), row tiles staged through a ring of shared-memory stages by
-// cp.async (barrier-bound, 24 us) and persistent warps with the next unit's
-// loads in flight (13.44 us, no gain).
+// and 14.2 us at 4 or 8; that stack now takes the bulk kernel).  Also
+// measured and dropped: 32-byte chunks (whole sector stores; 150+ registers,
+// 20.9 us against 16.9 us for that build's 16-byte chunks), row tiles staged
+// through a ring of shared-memory stages by cp.async (barrier-bound, 24 us)
+// and persistent warps with the next unit's loads in flight (13.44 us, no
+// gain).
 struct ChunkPlan {
     bool ok;
     int cpw;
@@ -424,6 +668,62 @@ static cudaError_t launch_chunks(const ExportArgs& a, int64_t tr, int64_t nc, cu
     return cudaGetLastError();
 }
 
+// The bulk kernel's staging must fit kBulkSmemMax (two CTAs per SM at
+// least; K up to 17,000 or so).
+constexpr int64_t kBulkSmemMax = 100 * 1024;
+
+
+// Rotate the bulk kernel's chunks (ROT) when, unrotated, the 16-byte shared
+// stores of eight consecutive lanes q would hit one unit 4 or more times:
+// unit ceil(q nb / 16) mod 8 (nb = 64, 128, 192, 256, 257, 320, 512, ...).
+static bool bulk_rotate(int64_t nb) {
+    int worst = 1;
+    for (int g = 0; g < 4; ++g) {
+        int cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int j = 0; j < 8; ++j) ++cnt[(((8 * g + j) * nb + 15) >> 4) & 7];
+        for (int u = 0; u < 8; ++u) worst = std::max(worst, cnt[u]);
+    }
+    return worst >= 4;
+}
+
+static bool bulk_fits(int64_t nb) { return bulk_smem_bytes(nb, bulk_rotate(nb)) <= kBulkSmemMax; }
+
+// Whether the bulk kernel beats the chunk kernel on `tiles` row tiles of nb
+// scale columns.  Few row tiles leave most SMs idle in the bulk kernel (one
+// CTA per tile).  Measured on GB300 with inputs larger than L2, bulk against
+// chunk: nb = 256 (rotated) 6.55 / 6.69 us at 304 tiles, 11.16 / 12.46 us at
+// 768, but 5.22 / 3.92 us at 152; nb = 225 and 240 (unrotated) even at 768
+// tiles (11.02 / 11.02 and 10.23 / 10.40 us), ahead at 1024 (12.8 / 13.4 us
+// for the MoE stack), behind at 512; nb = 100 behind up to 768 tiles.
+static bool bulk_wins(int64_t nb, int64_t tiles) {
+    if (!bulk_fits(nb)) return false;
+    return bulk_rotate(nb) ? tiles >= 304 : nb >= 192 && tiles >= 768;
+}
+
+// Dynamic shared memory above the 48 KB default, and the carveout: all of
+// it for shared memory when the launch stages tiles (five CTAs of the MoE
+// stack's 43.6 KB per SM), the default otherwise (the chunk kernel's loads
+// go through L1).  Both are per-kernel settings, so every launch sets them.
+template <typename F>
+static cudaError_t allow_smem(F* kernel, int64_t smem) {
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                smem > 0 ? (int)cudaSharedmemCarveoutMaxShared : (int)cudaSharedmemCarveoutDefault);
+}
+
+template <bool ROT>
+static cudaError_t launch_bulk(const ExportArgs& a, int64_t tr, cudaStream_t s) {
+    const int64_t smem = bulk_smem_bytes(ceil_div(a.K, 32), ROT);
+    const cudaError_t e = allow_smem(bulk_export_kernel<ROT>, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = tr < (int64_t(1) << 24) ? tr : (int64_t(1) << 24);  // one CTA per row tile
+    bulk_export_kernel<ROT><<<(unsigned)grid, kBulkThreads, (size_t)smem, s>>>(a, tr);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_export(const ExportArgs& a, cudaStream_t s) {
     const int64_t nb = ceil_div(a.K, 32);
     if (a.lay == 2) {
@@ -431,6 +731,8 @@ cudaError_t launch_export(const ExportArgs& a, cudaStream_t s) {
         const int64_t tr = ceil_div(a.rows, 128);
         const bool vin = (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0;
         const ChunkPlan p = chunk_plan(a);
+        if (p.ok && bulk_wins(nb, tr))
+            return bulk_rotate(nb) ? launch_bulk<true>(a, tr, s) : launch_bulk<false>(a, tr, s);
         if (p.ok) return p.cpw == 1 ? launch_chunks<1>(a, tr, p.nc, s) : launch_chunks<2>(a, tr, p.nc, s);
         const int64_t smem = (ct + 1) * kTileWords * 4 + ((nb + 3) & ~int64_t(3)) * 4;
         // nb > 4: a word of compact output then meets at most one row boundary
@@ -466,13 +768,23 @@ cudaError_t launch_export(const ExportArgs& a, cudaStream_t s) {
 cudaError_t launch_export_grouped(const GroupedExport& b0, cudaStream_t s) {
     if (b0.count <= 0) return cudaSuccess;
     GroupedExport b = b0;
-    int64_t gx = 1, gy = 1, warps1 = 0;
+    int64_t gx = 1, gy = 1, warps1 = 0, chunk_tiles = 0, smem = 0;
     for (int i = 0; i < b.count; ++i) {
         ExportArgs& a = b.item[i];
         const ChunkPlan p = chunk_plan(a);
         a.path = p.ok ? 1 : 0;
         gx = std::max(gx, ceil_div(a.rows, 128));
-        if (p.ok) warps1 += ceil_div(a.rows, 128) * p.nc;
+        if (p.ok) chunk_tiles += ceil_div(a.rows, 128);
+    }
+    // a storage takes the bulk path when the launch's chunk-path storages,
+    // one CTA per row tile, fill the GPU as one export of that width would
+    for (int i = 0; i < b.count; ++i) {
+        ExportArgs& a = b.item[i];
+        if (a.path == 1 && bulk_wins(ceil_div(a.K, 32), chunk_tiles)) {
+            a.path = bulk_rotate(ceil_div(a.K, 32)) ? 3 : 2;
+            smem = std::max(smem, bulk_smem_bytes(ceil_div(a.K, 32), a.path == 3));
+        }
+        if (a.path == 1) warps1 += ceil_div(a.rows, 128) * chunk_plan(a).nc;
     }
     const int cpw = warps1 <= (int64_t)sm_count() * 8 ? 2 : 1;
     for (int i = 0; i < b.count; ++i) {
@@ -484,10 +796,12 @@ cudaError_t launch_export_grouped(const GroupedExport& b0, cudaStream_t s) {
     const int64_t cap = (int64_t)sm_count() * 64;
     if (gx > cap) gx = cap;
     const dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)b.count);
+    cudaError_t e = cpw == 1 ? allow_smem(grouped_export_kernel<1>, smem) : allow_smem(grouped_export_kernel<2>, smem);
+    if (e != cudaSuccess) return e;
     if (cpw == 1)
-        grouped_export_kernel<1><<<grid, kChunkThreads, 0, s>>>(b);
+        grouped_export_kernel<1><<<grid, kChunkThreads, (size_t)smem, s>>>(b);
     else
-        grouped_export_kernel<2><<<grid, kChunkThreads, 0, s>>>(b);
+        grouped_export_kernel<2><<<grid, kChunkThreads, (size_t)smem, s>>>(b);
     return cudaGetLastError();
 }
 

@@ -684,22 +684,46 @@ def test_export_chunk_path_every_scale_count(mx, rows):
             np.testing.assert_array_equal(host_bits(o).reshape(rows, nb), want, err_msg=f"rows {rows} nb {nb}")
 
 
-@pytest.mark.parametrize("nb", [16, 17, 63, 225, 256, 300, 600, 1023])
-def test_export_staged_pipeline(mx, nb):
-    """Exports of more than two row tiles per SM take the persistent kernel
-    that stages row tiles in shared memory (7, 4 or 2 stages by tile size;
-    nb = 1023 no longer fits and takes the chunk kernel): random swizzled
-    bytes, a ragged last row tile, equal to the oracle's export."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    rows = (2 * sms + 1) * 128 + 77
+@pytest.mark.parametrize("nb", [16, 17, 63, 64, 128, 225, 240, 256, 257, 300, 512, 600, 1023])
+def test_export_bulk_path(mx, nb):
+    """Large swizzled exports take the bulk kernel (each row tile staged in
+    shared memory by one bulk copy, its compact rows written back by one
+    bulk store per 64-row part): 801 row tiles, so widths with the rotated
+    chunk order (63, 64, 128, 256, 257, 512; 63 and 257 also take the
+    separate row-crossing step) and unrotated widths of 192 columns or more
+    (225, 240, 300) go bulk, while 16 and 17 (narrow, unrotated) and 600 and
+    1023 (staging too large) stay on the chunk kernel.  The last row tile
+    is ragged (77 rows: its second part holds 13 rows, and rows x nb ends
+    off a 16-byte boundary for odd nb); random swizzled bytes.  Equal to the
+    oracle's export, written at the start of its buffer and 16 bytes into
+    one, with the bytes around it untouched; the same weight split into
+    three storages through the grouped export likewise."""
+    rows = 800 * 128 + 77
     K = 32 * nb - 5
     sw = _random_swizzled(rows, K, seed=nb)
+    want = oracle.export_scales(sw, oracle.SWIZZLED, rows, K)
     d = torch.from_numpy(sw).cuda()
-    comp = mx.export_mxfp8(torch.empty((rows, K), dtype=torch.uint8, device="cuda"), d, shape=(rows, K),
-                           layout="swizzled")
+    payload = torch.empty((rows, K), dtype=torch.uint8, device="cuda")  # aliased by the export, never read
+    comp = mx.export_mxfp8(payload, d, shape=(rows, K), layout="swizzled")
+    raw = torch.full((rows * nb + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+    c16 = mx.export_mxfp8(payload, d, shape=(rows, K), layout="swizzled", scale_out=raw[16:16 + rows * nb])
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(host_bits(comp.scale_inv).reshape(rows, nb),
-                                  oracle.export_scales(sw, oracle.SWIZZLED, rows, K))
+    np.testing.assert_array_equal(host_bits(comp.scale_inv).reshape(rows, nb), want)
+    np.testing.assert_array_equal(host_bits(c16.scale_inv).reshape(rows, nb), want)
+    r = host_bits(raw)
+    assert (r[:16] == 0xA5).all() and (r[16 + rows * nb:] == 0xA5).all()
+    # the same weight as three storages, split at row tiles (each piece a
+    # swizzled buffer of its own): the grouped kernel's bulk path
+    ct = (nb + 3) // 4
+    cuts = [0, 250 * 128, 600 * 128, rows]
+    items = [{"data": payload[a:b], "scales": d[(a // 128) * ct * 512:((b + 127) // 128) * ct * 512],
+              "shape": (b - a, K), "layout": "swizzled"} for a, b in zip(cuts, cuts[1:])]
+    gout = torch.full((rows * nb + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+    mx.export_mxfp8_grouped(items, scale_out=gout[16:16 + rows * nb])
+    torch.cuda.synchronize()
+    g = host_bits(gout)
+    np.testing.assert_array_equal(g[16:16 + rows * nb].reshape(rows, nb), want)
+    assert (g[:16] == 0xA5).all() and (g[16 + rows * nb:] == 0xA5).all()
 
 
 def test_export_chunk_path_past_65535_row_tiles(mx):
@@ -751,6 +775,31 @@ def test_grouped_export_matches_single_exports(mx):
         assert c.is_view == (lay == "compact" or (lay == "padded" and nb % 4 == 0))
         assert c.data.data_ptr() == st["data"].data_ptr()
     assert mx.export_mxfp8_grouped([]) == []
+
+
+def test_grouped_bulk_export_many_tiles_per_cta(mx):
+    """The grouped kernel's bulk path walks a storage's row tiles with a
+    grid stride capped at 64 CTAs per SM, so a storage of more row tiles
+    takes several per CTA through one mbarrier's alternating phases:
+    1,300,000 rows x 64 scale columns (10,157 row tiles, rotated chunk
+    order, random swizzled bytes), beside a storage of 100 scale columns
+    (unrotated and narrow: the chunk path).  Equal to the oracle's export."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows, K = 1_300_000, 2048
+    assert (rows + 127) // 128 > 64 * sms
+    sw = _random_swizzled(rows, K, seed=64)
+    small_rows, small_K = 300, 3195
+    small_sw = _random_swizzled(small_rows, small_K, seed=7)
+    items = [{"data": torch.empty((rows, K), dtype=torch.uint8, device="cuda"),  # aliased, never read
+              "scales": torch.from_numpy(sw).cuda(), "shape": (rows, K), "layout": "swizzled"},
+             {"data": torch.empty((small_rows, small_K), dtype=torch.uint8, device="cuda"),
+              "scales": torch.from_numpy(small_sw).cuda(), "shape": (small_rows, small_K), "layout": "swizzled"}]
+    comps = mx.export_mxfp8_grouped(items)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host_bits(comps[0].scale_inv).reshape(rows, -1),
+                                  oracle.export_scales(sw, oracle.SWIZZLED, rows, K))
+    np.testing.assert_array_equal(host_bits(comps[1].scale_inv).reshape(small_rows, -1),
+                                  oracle.export_scales(small_sw, oracle.SWIZZLED, small_rows, small_K))
 
 
 def test_grouped_export_past_one_launch(mx):
