@@ -309,6 +309,69 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_
     }
 }
 
+// The projection of fp32 input, K % 32 == 0, 32-byte aligned input and
+// output rows: four lanes share a 1x32 block, each with 8 elements -- one
+// 32-byte load, one 32-byte store -- so a warp's load and store each cover
+// 1 KB of contiguous memory (8 blocks).  With a lane per block the 128 bytes
+// a lane reads and writes made every load and store instruction touch 32
+// separate lines: 86.4 against 77.7 us on 8192 x 8192 fp32.  The block's
+// amax joins over its four lanes by two shuffles (the lane units are a
+// multiple of 4, and so is the grid stride, so a block's four lanes are
+// always active together); each lane then projects its 8 elements with
+// rowwise_kernel's arithmetic.  The read-heavy fp32 forms (MXFP8, packed
+// MXFP4) keep a lane per block: four lanes repeat the block's exponent,
+// table and scale work, and with 1-8 units a thread in flight they ran at
+// 59.9 / 55.8 us or more against 53.4 / 48.8 us.
+__global__ void __launch_bounds__(kThreads) project_f32_quad_kernel(RowwiseArgs a, int64_t nb, int64_t step_r,
+                                                                    int64_t step_c) {
+    const int64_t nq = a.rows * nb * 4;  // lanes: 4 per block
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t S = (int64_t)gridDim.x * kThreads;  // step_r rows + step_c blocks
+    if (a.skip != nullptr && *a.skip != 0) return;  // skip-update request: write nothing
+    const unsigned gmask = 0xFu << (threadIdx.x & 28);  // the block's four lanes
+    const int p = (int)(tid & 3);                       // elements 8 p .. 8 p + 7 of each block
+    int64_t r = (tid >> 2) / nb, j = (tid >> 2) - r * nb;
+    for (int64_t tq = tid; tq < nq; tq += S) {
+        uint32_t v[8];
+        ld32(v, static_cast<const char*>(a.x) + (r * a.ldx + j * 32 + 8 * p) * 4);
+        uint32_t m = 0u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m = f32_absmax(m, v[k]);
+        m &= 0x7FFFFFFFu;  // magnitude patterns: NaN > Inf > finite
+        m = max(m, __shfl_xor_sync(gmask, m, 1));
+        m = max(m, __shfl_xor_sync(gmask, m, 2));
+        const bool poisoned = m >= 0x7F800000u;
+        const int e = block_exponent<23>(m);
+        const uint32_t mult = f32_pow2(-e), scl = f32_pow2(e);
+        const bool top = e == 125;  // only there can |x| / 2^e round past 6
+        uint32_t y[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            uint32_t t = f32_grid(v[k], mult);
+            if (top) t = f32_sat(t);
+            y[k] = poisoned ? 0x7FC00000u : (f32_mul(t, scl) | (v[k] & 0x80000000u));
+        }
+        st32(static_cast<char*>(a.y) + (r * a.ldy + j * 32 + 8 * p) * 4, y);
+        j += step_c;
+        r += step_r;
+        if (j >= nb) {
+            j -= nb;
+            r += 1;
+        }
+    }
+}
+
+cudaError_t launch_project_f32_quad(const RowwiseArgs& a, cudaStream_t s) {
+    const int64_t nb = a.K / 32;
+    int64_t grid = ceil_div(a.rows * nb * 4, (int64_t)kThreads);
+    const int64_t cap = (int64_t)1 << 30;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    const int64_t sb = grid * kThreads / 4;  // blocks per grid stride
+    project_f32_quad_kernel<<<(unsigned)grid, kThreads, 0, s>>>(a, nb, sb / nb, sb % nb);
+    return cudaGetLastError();
+}
+
 template <RowMode MODE, Elt ELT, bool VEC, int DST>
 cudaError_t launch_one(const RowwiseArgs& a, cudaStream_t s) {
     const int64_t nb = (a.K + 31) / 32;
@@ -347,6 +410,10 @@ cudaError_t dispatch(const RowwiseArgs& a, cudaStream_t s) {
     using T = Traits<ELT>;
     // vector path: every 32-byte segment of the input (and projection output) is aligned
     bool vec = aligned(a.x, 32) && (a.ldx * T::ES) % 32 == 0 && (a.K * T::ES) % 32 == 0;
+    if constexpr (ELT == Elt::FP32 && MODE == RowMode::PROJECT) {
+        // whole blocks, aligned input and output rows: four lanes per block
+        if (vec && a.K % 32 == 0 && aligned(a.y, 32) && (a.ldy * 4) % 32 == 0) return launch_project_f32_quad(a, s);
+    }
     if constexpr (MODE == RowMode::PROJECT) {
         vec = vec && aligned(a.y, 32) && (a.ldy * T::ES) % 32 == 0;
         return vec ? launch_one<MODE, ELT, true, 0>(a, s) : launch_one<MODE, ELT, false, 0>(a, s);
