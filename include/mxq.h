@@ -263,6 +263,11 @@ typedef struct {
  * copies them into `scale_out`, dropping padding and undoing the swizzle.
  *   scale_out: device buffer of scale_out_bytes >= rows*nb, used only when
  *              a copy is needed (may be NULL otherwise).
+ * Large swizzled copies stage 128-row tiles in shared memory through bulk
+ * copies whose completion the kernel waits for at most about a second; a
+ * tile whose copy has not arrived by then (a device fault, never expected)
+ * has its compact rows written as 0xFF, the E8M0 NaN code, since the call
+ * itself has already returned.
  * Errors: NO_ROWWISE_DATA if st->data is NULL (with rows*K > 0);
  * BUFFER_TOO_SMALL if a copy is needed and scale_out is NULL or too small;
  * INVALID_ARG otherwise.  `out` is written only on MXQ_OK. */
