@@ -114,6 +114,20 @@ __device__ __forceinline__ uint32_t lop_select(uint32_t a, uint32_t b, uint32_t 
     return (a & mask) | (b & ~mask);
 }
 
+// Row and block of a flattened (row, block) index: q = i / n, i - q n, by one
+// 32-bit division when both fit in 32 bits (the usual case; a 64-bit division
+// is several times longer), else by a 64-bit one.
+__device__ __forceinline__ void split_index(int64_t i, int64_t n, int64_t& q, int64_t& rem) {
+    if ((((uint64_t)i | (uint64_t)n) >> 32) == 0) {
+        const uint32_t q32 = (uint32_t)i / (uint32_t)n;
+        q = q32;
+        rem = (int64_t)((uint32_t)i - q32 * (uint32_t)n);
+    } else {
+        q = i / n;
+        rem = i - q * n;
+    }
+}
+
 // ------------------------------------------------------ block scale rule
 
 // e = clamp(ceil(log2(amax/6)), -126, 125) from the magnitude pattern of a

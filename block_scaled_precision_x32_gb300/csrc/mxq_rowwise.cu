@@ -159,7 +159,8 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(RowwiseArgs a, int64_
     const int64_t total = a.rows * nb;
     const int64_t Cp = (nb + 3) & ~int64_t(3);
     if (a.skip != nullptr && *a.skip != 0) return;  // skip-update request: write nothing
-    int64_t r = tid / nb, j = tid - (tid / nb) * nb;
+    int64_t r, j;
+    split_index(tid, nb, r, j);
 
     for (int64_t w = tid; w < total; w += S) {
         const int64_t col0 = j * 32;
@@ -330,7 +331,8 @@ __global__ void __launch_bounds__(kThreads) project_f32_quad_kernel(RowwiseArgs 
     if (a.skip != nullptr && *a.skip != 0) return;  // skip-update request: write nothing
     const unsigned gmask = 0xFu << (threadIdx.x & 28);  // the block's four lanes
     const int p = (int)(tid & 3);                       // elements 8 p .. 8 p + 7 of each block
-    int64_t r = (tid >> 2) / nb, j = (tid >> 2) - r * nb;
+    int64_t r, j;
+    split_index(tid >> 2, nb, r, j);
     for (int64_t tq = tid; tq < nq; tq += S) {
         uint32_t v[8];
         ld32(v, static_cast<const char*>(a.x) + (r * a.ldx + j * 32 + 8 * p) * 4);
