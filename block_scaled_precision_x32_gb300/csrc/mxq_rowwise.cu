@@ -15,6 +15,8 @@
 // Misaligned or ragged views use the same code with element-wise loads.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "mxq_device.cuh"
 #include "mxq_internal.h"
 
@@ -499,11 +501,19 @@ cudaError_t launch_one(const RowwiseArgs& a, cudaStream_t s) {
     // MXFP8 / MXFP4 54.0 / 49.2 us against 57.3 / 52.0 us at 4 x resident);
     // the read-heavy bf16 MXFP8 and MXFP4 forms with 4 x the resident grid,
     // about two blocks per thread (32.3 / 27.1 us against 34.5 / 29.6 us
-    // resident, 34.9 / 27.7 us one per thread).  (Aligned fp32 views with
-    // K % 32 == 0 take the four- and two-lane kernels above instead.)
+    // resident, 34.9 / 27.7 us one per thread).  Larger tensors want the grid
+    // to grow with them: about 3 (MXFP8) or 2 (MXFP4) blocks per thread, never
+    // fewer CTAs than 4 x resident (MoE stack 32 x 4096 x 7184: MXFP8 449.5 ->
+    // 406.8 us, MXFP4 362.2 -> 330.7 us; 32768 x 16384: 248.3 -> 228.8 us and
+    // 203.5 -> 189.7 us; 8192 x 8192 keeps 4 x resident).  (Aligned fp32 views
+    // with K % 32 == 0 take the four- and two-lane kernels above instead.)
     int64_t grid = ceil_div(total, (int64_t)kThreads);
     const bool one_per_thread = MODE == RowMode::PROJECT || ELT == Elt::FP32;
-    const int64_t cap = one_per_thread ? ((int64_t)1 << 30) : (int64_t)sm_count() * occ * 4;
+    int64_t cap = (int64_t)1 << 30;
+    if (!one_per_thread) {
+        const int64_t bpt = MODE == RowMode::MXFP4 ? 2 : 3;  // blocks per thread
+        cap = std::min(std::max((int64_t)sm_count() * occ * 4, ceil_div(total, (int64_t)kThreads * bpt)), cap);
+    }
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     const int64_t stride = grid * kThreads;
