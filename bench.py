@@ -753,8 +753,8 @@ def run_e2e(args, lib, dev, x_host, world, chunks: int = 2):
 
 PROFILE_NAMES = ("projection", "mxfp8_row", "block128", "dequant_bf16", "export", "mxfp8_col",
                  "mxfp8_col_dequant_bf16", "mxfp8_col_dequant_fp32", "mxfp4_pack", "mxfp4_dequant_bf16", "dequant_fp32",
-                 "dequant_block128_bf16", "quantize_export", "fp32_block128", "fp32_mxfp8_col", "moe_export",
-                 "moe_grouped_export")
+                 "dequant_block128_bf16", "dequant_block128_fp32", "quantize_export", "fp32_block128", "fp32_mxfp8_col",
+                 "moe_export", "moe_grouped_export")
 
 
 def run_profile(name: str, reps: int = 3):
@@ -818,11 +818,11 @@ def run_profile(name: str, reps: int = 3):
                 out = torch.empty((ROWS, COLS), dtype=torch.bfloat16 if name == "dequant_bf16" else torch.float32,
                                   device=dev)
                 call = lib.plan_dequantize(d, out, scales=s, layout="swizzled")
-        elif name == "dequant_block128_bf16":
+        elif name in ("dequant_block128_bf16", "dequant_block128_fp32"):
             d, s = lib.fp8_block128_direct(x)
             del x
-            call = lib.plan_dequantize(d, torch.empty((ROWS, COLS), dtype=torch.bfloat16, device=dev),
-                                       tile_scale_inv=s)
+            odt = torch.bfloat16 if name == "dequant_block128_bf16" else torch.float32
+            call = lib.plan_dequantize(d, torch.empty((ROWS, COLS), dtype=odt, device=dev), tile_scale_inv=s)
         elif name in ("mxfp8_col_dequant_bf16", "mxfp8_col_dequant_fp32"):
             d, s = lib.mxfp8_col_direct(x, "swizzled")
             del x

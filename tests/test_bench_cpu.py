@@ -46,6 +46,11 @@ def test_algorithmic_bytes():
     assert bench.BYTES["export"] == 2 * 8192 * 256
     assert bench.STEP_BYTES == 880_820_224
     assert bench.EXTRA_BYTES["dequant_fp32"] == 5 * n + n // 32
+    assert bench.EXTRA_BYTES["mxfp8_col_dequant_fp32"] == 5 * n + n // 32
+    assert bench.EXTRA_BYTES["dequant_block128_fp32"] == 5 * n + 4 * 64 * 64
+    # every timed conversion names the source its kernel is built from and has a --profile driver
+    for name in list(bench.BYTES) + list(bench.EXTRA_BYTES):
+        assert name in bench.KERNEL_FILES and name in bench.PROFILE_NAMES, name
 
 
 def test_traffic_record_matches_the_kernel_sources():
