@@ -783,23 +783,27 @@ def test_grouped_bulk_export_many_tiles_per_cta(mx):
     takes several per CTA through one mbarrier's alternating phases:
     1,300,000 rows x 64 scale columns (10,157 row tiles, rotated chunk
     order, random swizzled bytes), beside a storage of 100 scale columns
-    (unrotated and narrow: the chunk path).  Equal to the oracle's export."""
+    (unrotated and narrow: the chunk path) and two small storages the bulk
+    path takes because the launch as a whole is large: one row of 225
+    columns (a single partial part, its bytes past the last 16-byte boundary
+    stored one by one) and 77 rows of 257 (rotated, with the row-crossing
+    step).  Equal to the oracle's export."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     rows, K = 1_300_000, 2048
     assert (rows + 127) // 128 > 64 * sms
     sw = _random_swizzled(rows, K, seed=64)
-    small_rows, small_K = 300, 3195
-    small_sw = _random_swizzled(small_rows, small_K, seed=7)
+    small = [(300, 3195), (1, 7184), (77, 32 * 257 - 9)]
+    small_sw = [_random_swizzled(r, k, seed=7 + i) for i, (r, k) in enumerate(small)]
     items = [{"data": torch.empty((rows, K), dtype=torch.uint8, device="cuda"),  # aliased, never read
-              "scales": torch.from_numpy(sw).cuda(), "shape": (rows, K), "layout": "swizzled"},
-             {"data": torch.empty((small_rows, small_K), dtype=torch.uint8, device="cuda"),
-              "scales": torch.from_numpy(small_sw).cuda(), "shape": (small_rows, small_K), "layout": "swizzled"}]
+              "scales": torch.from_numpy(sw).cuda(), "shape": (rows, K), "layout": "swizzled"}]
+    items += [{"data": torch.empty((r, k), dtype=torch.uint8, device="cuda"), "scales": torch.from_numpy(t).cuda(),
+               "shape": (r, k), "layout": "swizzled"} for (r, k), t in zip(small, small_sw)]
     comps = mx.export_mxfp8_grouped(items)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(host_bits(comps[0].scale_inv).reshape(rows, -1),
                                   oracle.export_scales(sw, oracle.SWIZZLED, rows, K))
-    np.testing.assert_array_equal(host_bits(comps[1].scale_inv).reshape(small_rows, -1),
-                                  oracle.export_scales(small_sw, oracle.SWIZZLED, small_rows, small_K))
+    for c, (r, k), t in zip(comps[1:], small, small_sw):
+        np.testing.assert_array_equal(host_bits(c.scale_inv).reshape(r, -1), oracle.export_scales(t, oracle.SWIZZLED, r, k))
 
 
 def test_grouped_export_past_one_launch(mx):
